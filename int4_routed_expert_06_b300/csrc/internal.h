@@ -1,0 +1,45 @@
+// Internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "moe_int4.h"
+
+namespace moe {
+
+struct Shape {
+    int H, E, k, I, Is, G;
+    int act, router, qscale; // moe_dtype values
+};
+
+// Record a thread-local message and return `st`.
+moe_status fail(moe_status st, const char *fmt, ...);
+moe_status cuda_check(cudaError_t e, const char *what);
+// Validate a config and copy it into `s` (may be NULL).
+moe_status check_config(const moe_config *c, Shape *s);
+
+// Router logits [T, E] and shared-gate logit [T].
+cudaError_t launch_router(const Shape &s, const void *x, int T, const void *w_router,
+                          const float *bias, const void *w_sg, float *logits, float *sg_logit,
+                          cudaStream_t st);
+// Top-k + renormalised softmax from logits [T, E].
+cudaError_t launch_topk(const Shape &s, const float *logits, int T, int32_t *idx, float *w,
+                        cudaStream_t st);
+// a[t, i, :] = silu(W_g x) * (W_u x) for the n_act active experts of each token.
+cudaError_t launch_gateup(const Shape &s, const void *x, int T, int k_eff, int n_act,
+                          const int32_t *topk_idx, const ExpertSrc &src, float *a, int Imax,
+                          cudaStream_t st);
+// y[t] = sum_i weight_i * W_d,i a[t, i, :].
+cudaError_t launch_down(const Shape &s, const float *a, int T, int k_eff, int n_act, int Imax,
+                        const int32_t *topk_idx, const float *topk_w, const float *gate_logit,
+                        const ExpertSrc &src, void *y, float *y32, cudaStream_t st);
+// Stable counting sort of (token, rank) pairs by expert.
+cudaError_t launch_bucket(const Shape &s, const int32_t *idx, int T, int32_t *counts,
+                          int32_t *offsets, int32_t *perm_tok, int32_t *perm_rank,
+                          int32_t *chunk_hist, cudaStream_t st);
+int bucket_chunks(int pairs);
+
+} // namespace moe

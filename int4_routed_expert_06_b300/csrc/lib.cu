@@ -1,0 +1,6 @@
+// Single translation unit of libmoe_int4.so: the per-device error word is one
+// __device__ variable shared by every kernel, so all sources compile together.
+#include "api.cu"
+#include "kernels_decode.cu"
+#include "bucket.cu"
+#include "slot_pool.cu"

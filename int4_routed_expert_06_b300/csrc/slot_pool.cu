@@ -1,0 +1,307 @@
+// Bounded HBM expert slot pool with LFU + recency eviction.
+//
+// The Swiftlet pages keep hot routed experts in a bounded pool of slots,
+// fetch a missing expert with one read of its fixed-stride blob, and evict by
+// "LFU plus recency" (page 2 "How it works" and "Relation to
+// TurboFieldfare").  Here the pool lives in HBM, the backing store is pinned
+// host memory, a fill is one cudaMemcpyAsync per expert on a side stream, and
+// the policy runs on the host:
+//   hit  -> use count + 1, stamp = lookup clock (one tick per lookup);
+//   miss -> lowest empty slot, else evict the expert not needed by this
+//           lookup with the smallest (use count, stamp, slot id); the filled
+//           slot starts at use count 1.
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+
+namespace {
+
+constexpr int kMaxUpdates = 32;
+
+struct TableUpdate {
+    int32_t n;
+    int32_t expert[kMaxUpdates];  // installed expert
+    int32_t slot[kMaxUpdates];    // its slot
+    int32_t evicted[kMaxUpdates]; // expert removed from that slot, -1 = none
+};
+
+// Device-table update for one layer: evictions first, then installs.
+__global__ void table_update_kernel(int32_t *__restrict__ row, int E, TableUpdate u)
+{
+    const int j = threadIdx.x;
+    if (j < u.n && u.evicted[j] >= 0 && u.evicted[j] < E)
+        row[u.evicted[j]] = -1;
+    __syncthreads();
+    if (j < u.n && u.expert[j] >= 0 && u.expert[j] < E)
+        row[u.expert[j]] = u.slot[j];
+}
+
+struct Fill {
+    int32_t expert, slot, evicted;
+};
+
+} // namespace
+
+struct slot_pool {
+    moe::Shape s;
+    int32_t L = 0, S = 0;
+    char *pool = nullptr;
+    const char *backing = nullptr;
+    size_t stride = 0, blob_bytes = 0;
+    cudaStream_t side = nullptr;
+    std::vector<int32_t> table;          // [L*E] expert -> slot
+    std::vector<int32_t> owner;          // [L*S] slot -> expert
+    std::vector<int64_t> freq, stamp;    // [L*S]
+    std::vector<std::vector<Fill>> pending; // per layer: fills of its last lookup
+    int64_t clock = 0;
+    int32_t *table_dev = nullptr;
+    moe_pool_stats st{};
+    std::mutex mu;
+};
+
+extern "C" moe_status slot_pool_create(const moe_config *cfg, int32_t n_layers, int32_t slots_per_layer,
+                                       void *pool_dev, size_t pool_bytes, const void *backing_host,
+                                       size_t expert_stride, cudaStream_t side_stream, slot_pool **out)
+{
+    using namespace moe;
+    if (!out)
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_create: out is NULL");
+    *out = nullptr;
+    Shape s;
+    moe_status cs = check_config(cfg, &s);
+    if (cs != MOE_OK)
+        return cs;
+    if (n_layers <= 0 || slots_per_layer <= 0)
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_create: n_layers and slots_per_layer must be > 0");
+    if (!pool_dev || (reinterpret_cast<uintptr_t>(pool_dev) & 255))
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_create: pool_dev must be non-NULL and 256-byte aligned");
+    if (!backing_host)
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_create: backing_host is NULL");
+    moe_blob_layout lay;
+    moe_blob_layout_get(cfg, cfg->inter, &lay);
+    if (expert_stride < lay.bytes || (expert_stride & 255))
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_create: expert_stride %zu must be a multiple of 256 and >= %zu",
+                    expert_stride, lay.bytes);
+    if (pool_bytes / expert_stride < (size_t)n_layers * slots_per_layer)
+        return fail(MOE_ERR_OOM, "slot_pool_create: pool_bytes %zu < %d layers x %d slots x %zu", pool_bytes,
+                    n_layers, slots_per_layer, expert_stride);
+    slot_pool *p = new (std::nothrow) slot_pool();
+    if (!p)
+        return fail(MOE_ERR_OOM, "slot_pool_create: host allocation failed");
+    p->s = s;
+    p->L = n_layers;
+    p->S = slots_per_layer;
+    p->pool = static_cast<char *>(pool_dev);
+    p->backing = static_cast<const char *>(backing_host);
+    p->stride = expert_stride;
+    p->blob_bytes = lay.bytes;
+    p->side = side_stream;
+    p->table.assign((size_t)n_layers * s.E, -1);
+    p->owner.assign((size_t)n_layers * slots_per_layer, -1);
+    p->freq.assign((size_t)n_layers * slots_per_layer, 0);
+    p->stamp.assign((size_t)n_layers * slots_per_layer, 0);
+    p->pending.resize(n_layers);
+    *out = p;
+    return MOE_OK;
+}
+
+// The device table is allocated (all -1) on first use, so that the host
+// policy needs no device work until something is filled or read.
+static moe_status ensure_table_dev(slot_pool *p)
+{
+    using namespace moe;
+    if (p->table_dev)
+        return MOE_OK;
+    const size_t tb = sizeof(int32_t) * (size_t)p->L * p->s.E;
+    int32_t *t = nullptr;
+    cudaError_t e = cudaMalloc(&t, tb);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(t, 0xFF, tb, p->side);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(p->side);
+    if (e != cudaSuccess) {
+        if (t)
+            cudaFree(t);
+        return cuda_check(e, "slot pool device table");
+    }
+    p->table_dev = t;
+    return MOE_OK;
+}
+
+extern "C" moe_status slot_pool_lookup(slot_pool *p, int32_t layer, const int32_t *expert_ids, int32_t n,
+                                       int32_t *slots_out, int32_t *miss_ids, int32_t *n_miss)
+{
+    using namespace moe;
+    if (!p || !n_miss || (n > 0 && (!expert_ids || !slots_out || !miss_ids)))
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_lookup: NULL argument");
+    if (layer < 0 || layer >= p->L || n < 0)
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_lookup: layer %d or n %d out of range", layer, n);
+    std::lock_guard<std::mutex> g(p->mu);
+    const int E = p->s.E, S = p->S;
+    std::vector<int32_t> uniq;
+    for (int j = 0; j < n; ++j) {
+        const int e = expert_ids[j];
+        if (e < 0 || e >= E)
+            return fail(MOE_ERR_INVALID_ARG, "slot_pool_lookup: expert id %d outside [0, %d)", e, E);
+        bool seen = false;
+        for (int u : uniq)
+            seen |= (u == e);
+        if (!seen)
+            uniq.push_back(e);
+    }
+    if ((int)uniq.size() > S)
+        return fail(MOE_ERR_POOL_EXHAUSTED, "slot_pool_lookup: %zu distinct experts, %d slots", uniq.size(), S);
+    p->clock += 1;
+    p->st.lookups += 1;
+    int32_t *tab = &p->table[(size_t)layer * E];
+    int32_t *own = &p->owner[(size_t)layer * S];
+    int64_t *fr = &p->freq[(size_t)layer * S];
+    int64_t *sp = &p->stamp[(size_t)layer * S];
+    std::vector<int32_t> missing;
+    for (int e : uniq) {
+        const int s = tab[e];
+        if (s >= 0) {
+            fr[s] += 1;
+            sp[s] = p->clock;
+            p->st.hits += 1;
+        } else {
+            missing.push_back(e);
+        }
+    }
+    std::vector<Fill> &fills = p->pending[layer];
+    fills.clear();
+    for (int e : missing) {
+        int s = -1;
+        for (int j = 0; j < S && s < 0; ++j)
+            if (own[j] < 0)
+                s = j;
+        int evicted = -1;
+        if (s < 0) {
+            for (int j = 0; j < S; ++j) {
+                bool needed = false;
+                for (int u : uniq)
+                    needed |= (own[j] == u);
+                if (needed)
+                    continue;
+                if (s < 0 || fr[j] < fr[s] || (fr[j] == fr[s] && sp[j] < sp[s]))
+                    s = j; // equal (count, stamp): the lower slot id, found first, stays
+            }
+            evicted = own[s];
+            tab[evicted] = -1;
+            p->st.evictions += 1;
+        }
+        own[s] = e;
+        tab[e] = s;
+        fr[s] = 1;
+        sp[s] = p->clock;
+        p->st.misses += 1;
+        fills.push_back({e, s, evicted});
+    }
+    for (int j = 0; j < n; ++j)
+        slots_out[j] = tab[expert_ids[j]];
+    *n_miss = (int32_t)fills.size();
+    for (size_t j = 0; j < fills.size(); ++j)
+        miss_ids[j] = fills[j].expert;
+    return MOE_OK;
+}
+
+extern "C" moe_status slot_pool_fill(slot_pool *p, int32_t layer, const int32_t *miss_ids, int32_t n_miss,
+                                     cudaEvent_t done)
+{
+    using namespace moe;
+    if (!p || (n_miss > 0 && !miss_ids))
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_fill: NULL argument");
+    if (layer < 0 || layer >= p->L)
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_fill: layer %d out of range", layer);
+    std::lock_guard<std::mutex> g(p->mu);
+    std::vector<Fill> &fills = p->pending[layer];
+    if ((size_t)n_miss != fills.size())
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_fill: %d misses given, last lookup of layer %d had %zu",
+                    n_miss, layer, fills.size());
+    for (int j = 0; j < n_miss; ++j)
+        if (miss_ids[j] != fills[j].expert)
+            return fail(MOE_ERR_INVALID_ARG, "slot_pool_fill: miss %d is expert %d, lookup assigned expert %d", j,
+                        miss_ids[j], fills[j].expert);
+    moe_status ts = ensure_table_dev(p);
+    if (ts != MOE_OK)
+        return ts;
+    const int E = p->s.E;
+    for (const Fill &f : fills) {
+        char *dst = p->pool + ((size_t)layer * p->S + f.slot) * p->stride;
+        const char *src = p->backing + ((size_t)layer * E + f.expert) * p->stride;
+        cudaError_t e = cudaMemcpyAsync(dst, src, p->blob_bytes, cudaMemcpyHostToDevice, p->side);
+        if (e != cudaSuccess)
+            return cuda_check(e, "slot_pool_fill: copy");
+        p->st.bytes_filled += (int64_t)p->blob_bytes;
+    }
+    for (size_t j0 = 0; j0 < fills.size(); j0 += kMaxUpdates) {
+        TableUpdate u{};
+        u.n = (int32_t)std::min(fills.size() - j0, (size_t)kMaxUpdates);
+        for (int j = 0; j < u.n; ++j) {
+            u.expert[j] = fills[j0 + j].expert;
+            u.slot[j] = fills[j0 + j].slot;
+            u.evicted[j] = fills[j0 + j].evicted;
+        }
+        table_update_kernel<<<1, kMaxUpdates, 0, p->side>>>(p->table_dev + (size_t)layer * E, E, u);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return cuda_check(e, "slot_pool_fill: table update");
+    }
+    fills.clear();
+    if (done) {
+        cudaError_t e = cudaEventRecord(done, p->side);
+        if (e != cudaSuccess)
+            return cuda_check(e, "slot_pool_fill: event record");
+    }
+    return MOE_OK;
+}
+
+extern "C" moe_status slot_pool_layer(slot_pool *p, int32_t layer, const int32_t **table_dev,
+                                      const void **pool_base_dev)
+{
+    using namespace moe;
+    if (!p || !table_dev || !pool_base_dev)
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_layer: NULL argument");
+    if (layer < 0 || layer >= p->L)
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_layer: layer %d out of range", layer);
+    std::lock_guard<std::mutex> g(p->mu);
+    moe_status ts = ensure_table_dev(p);
+    if (ts != MOE_OK)
+        return ts;
+    *table_dev = p->table_dev + (size_t)layer * p->s.E;
+    *pool_base_dev = p->pool + (size_t)layer * p->S * p->stride;
+    return MOE_OK;
+}
+
+extern "C" moe_status slot_pool_table_host(slot_pool *p, int32_t layer, int32_t *table_host)
+{
+    using namespace moe;
+    if (!p || !table_host)
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_table_host: NULL argument");
+    if (layer < 0 || layer >= p->L)
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_table_host: layer %d out of range", layer);
+    std::lock_guard<std::mutex> g(p->mu);
+    for (int e = 0; e < p->s.E; ++e)
+        table_host[e] = p->table[(size_t)layer * p->s.E + e];
+    return MOE_OK;
+}
+
+extern "C" moe_status slot_pool_stats(slot_pool *p, moe_pool_stats *out)
+{
+    using namespace moe;
+    if (!p || !out)
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_stats: NULL argument");
+    std::lock_guard<std::mutex> g(p->mu);
+    *out = p->st;
+    return MOE_OK;
+}
+
+extern "C" void slot_pool_destroy(slot_pool *p)
+{
+    if (!p)
+        return;
+    if (p->table_dev)
+        cudaFree(p->table_dev);
+    delete p;
+}

@@ -1,0 +1,185 @@
+"""GPU parity of the decode path against the CPU oracle, through the C-ABI.
+
+Routing indices are compared bit-exactly, outputs within the stated
+tolerance; workloads are the tiny layer and the 35B- and 80B-shaped layers at
+their full sizes, in the launch configuration the bench times (T = 1).
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import TOL, assert_close, device_layer, layer_forward, layer_of, near_tie_tokens, workspace
+from int4_routed_expert_06_b300 import binding as B
+from int4_routed_expert_06_b300 import synth
+from oracle import oracle as O
+
+pytestmark = pytest.mark.gpu
+
+NAMES = ["tiny", "35b-dec", "80b-dec"]
+
+
+def _xs(name, n):
+    shape = synth.SHAPES[name]
+    if name == "tiny":
+        return synth.make_x(shape, synth.TINY_X_SEED, device="cuda")
+    return synth.decode_xs(shape, n, device="cuda")
+
+
+def _route(dl, x, w):
+    shape = dl.shape
+    T = x.shape[0]
+    idx = torch.empty((T, shape.top_k), dtype=torch.int32, device="cuda")
+    tw = torch.empty((T, shape.top_k), dtype=torch.float32, device="cuda")
+    sg = torch.empty((T,), dtype=torch.float32, device="cuda")
+    lg = torch.empty((T, shape.n_experts), dtype=torch.float32, device="cuda")
+    rep = dl.replicas[0]
+    B.moe_route(dl.cfg, x, T, rep["w_router"], rep["router_bias"], rep["w_shared_gate"], idx, tw, sg, lg)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), tw.cpu().numpy(), sg.cpu().numpy(), lg.cpu().numpy()
+
+
+@pytest.mark.parametrize("name", NAMES)
+@pytest.mark.parametrize("T", [1, 13, 64])
+def test_route_parity(name, T):
+    shape, w, L = layer_of(name)
+    dl = device_layer(name)
+    x = _xs(name, 64)[:T] if name != "tiny" else _xs(name, 4)[: min(T, 4)]
+    idx, tw, sg, lg = _route(dl, x, w)
+    ref_lg, ref_s, ref_idx, ref_w = L.route(x)
+    scale = np.abs(ref_lg).max()
+    np.testing.assert_allclose(lg, ref_lg, rtol=0, atol=2e-5 * scale)
+    np.testing.assert_allclose(sg, ref_s, rtol=0, atol=2e-5 * max(1.0, np.abs(ref_s).max()))
+    tie = near_tie_tokens(ref_lg, shape.top_k)
+    assert tie.sum() <= max(1, len(x) // 50), "too many near-ties for a seeded workload"
+    np.testing.assert_array_equal(idx[~tie], ref_idx[~tie])
+    # selection and weights on the GPU's own fp32 logits: exact selection
+    own_idx, own_w = O.topk(lg.astype(np.float64), shape.top_k)
+    np.testing.assert_array_equal(idx, own_idx)
+    np.testing.assert_allclose(tw, own_w, rtol=2e-6, atol=1e-7)
+    np.testing.assert_allclose(tw.sum(axis=1), 1.0, rtol=1e-5)
+
+
+def test_topk_ties_and_k_equals_e_on_device():
+    """Exact ties pick the lower expert id; k = E gives a full softmax order."""
+    cfg = B.config_for(synth.TINY)
+    cfg.top_k = 8
+    H, E = 64, 8
+    x = torch.zeros((2, H), device="cuda")
+    x[:, 0] = 1.0
+    wr = torch.zeros((E, H), device="cuda")
+    wr[:, 0] = torch.tensor([1.0, 3.0, 3.0, 2.0, 3.0, -1.0, 0.5, 3.0])
+    wsg = torch.zeros(H, device="cuda")
+    idx = torch.empty((2, 8), dtype=torch.int32, device="cuda")
+    tw = torch.empty((2, 8), device="cuda")
+    sg = torch.empty(2, device="cuda")
+    B.moe_route(cfg, x, 2, wr, None, wsg, idx, tw, sg)
+    torch.cuda.synchronize()
+    assert idx[0].tolist() == [1, 2, 4, 7, 3, 0, 6, 5]
+    ref_idx, ref_w = O.topk(wr[:, 0].double().cpu().numpy(), 8)
+    np.testing.assert_allclose(tw[0].cpu().numpy(), ref_w, rtol=1e-6)
+    cfg.top_k = 1
+    B.moe_route(cfg, x, 2, wr, None, wsg, idx, tw, sg)
+    torch.cuda.synchronize()
+    assert idx[0, 0].item() == 1 and tw[0, 0].item() == 1.0
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_layer_decode_parity(name):
+    """T = 1 decode steps, each its own call (the bench's configuration)."""
+    shape, w, L = layer_of(name)
+    dl = device_layer(name)
+    xs = _xs(name, 6)
+    steps = range(len(xs)) if name == "tiny" else range(6)
+    for s in steps:
+        x = xs[s:s + 1]
+        y, y32, idx, tw = layer_forward(dl, x)
+        ref = L.forward(x)
+        tie = near_tie_tokens(ref["logits"], shape.top_k)
+        if tie[0]:
+            continue
+        np.testing.assert_array_equal(idx.cpu().numpy(), ref["idx"])
+        assert_close(y32.cpu().numpy(), ref["y"], shape.act, f"{name} step {s} y_f32")
+        assert_close(y.float().cpu().numpy(), ref["y"], shape.act, f"{name} step {s} y")
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 4), ("35b-dec", 5), ("80b-dec", 3)])
+def test_layer_batched_tokens(name, T):
+    """Several tokens in one call (ragged, not a multiple of any tile)."""
+    shape, w, L = layer_of(name)
+    dl = device_layer(name)
+    x = _xs(name, 8)[:T]
+    y, y32, idx, tw = layer_forward(dl, x)
+    ref = L.forward(x)
+    ok = ~near_tie_tokens(ref["logits"], shape.top_k)
+    np.testing.assert_array_equal(idx.cpu().numpy()[ok], ref["idx"][ok])
+    assert_close(y32.cpu().numpy()[ok], ref["y"][ok], shape.act, f"{name} T={T}")
+
+
+@pytest.mark.parametrize("name", ["tiny", "80b-dec"])
+def test_expert_forward_parity(name):
+    shape, w, L = layer_of(name)
+    T = 3
+    x = _xs(name, 4)[:T] if name != "tiny" else _xs(name, 4)[:T]
+    for e in (0, shape.n_experts - 1):
+        ex = B.expert_struct(w, e)
+        y = torch.empty((T, shape.hidden), dtype=synth.torch_dtype(shape.act), device="cuda")
+        y32 = torch.empty((T, shape.hidden), device="cuda")
+        nb = B.moe_expert_workspace_bytes(dl_cfg := B.config_for(shape), T)
+        ws = workspace(nb)
+        B.moe_expert_forward(dl_cfg, ex, shape.inter, x, T, y, y32, ws, nb)
+        torch.cuda.synchronize()
+        view = O.ExpertView(w, e)
+        ref = np.stack([O.expert(view, shape.group, x[t]) for t in range(T)])
+        assert_close(y32.cpu().numpy(), ref, shape.act, f"expert {e}")
+
+
+def test_pool_placement_never_changes_the_result():
+    """The same layer behind two different slot tables gives bit-identical y."""
+    name = "80b-dec"
+    a, b = device_layer(name, 0), device_layer(name, -1)
+    xs = _xs(name, 4)
+    for s in range(4):
+        ya = layer_forward(a, xs[s:s + 1])
+        yb = layer_forward(b, xs[s:s + 1])
+        assert torch.equal(ya[0], yb[0]) and torch.equal(ya[1], yb[1]) and torch.equal(ya[2], yb[2])
+
+
+def test_missing_slot_is_reported_not_faulted():
+    name = "tiny"
+    shape, w, L = layer_of(name)
+    dl = B.DeviceLayer(shape, w, synth.shuffled_slots(shape.n_experts, 3))
+    x = _xs(name, 4)
+    ref = L.forward(x)
+    gone = int(ref["idx"][0, 0])
+    dl.replicas[0]["slots"][gone] = -1
+    T = x.shape[0]
+    y = torch.empty((T, shape.hidden), device="cuda")
+    nb = B.moe_layer_workspace_bytes(dl.cfg, T)
+    B.moe_layer_forward(dl.cfg, dl.struct(), x, T, y, workspace=workspace(nb), ws_bytes=nb)
+    assert B.moe_get_device_error() == B.MOE_ERR_NOT_RESIDENT
+    assert torch.isfinite(y).all()
+    assert B.moe_get_device_error() == 0          # read-and-clear
+
+
+@pytest.mark.parametrize("T,k,E", [(1, 10, 512), (97, 8, 256), (4096, 10, 512), (3000, 2, 8)])
+def test_bucket_parity(T, k, E):
+    rng = np.random.default_rng(T)
+    p = 1.0 / np.arange(1, E + 1) ** 1.1
+    p /= p.sum()
+    idx = np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    cfg = B.config_for(synth.DEC_80B)
+    cfg.n_experts, cfg.top_k = E, k
+    d_idx = torch.from_numpy(idx).cuda()
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    pt = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    pr = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    nb = B.moe_bucket_workspace_bytes(cfg, T)
+    B.moe_bucket(cfg, d_idx, T, counts, offsets, pt, pr, workspace(nb), nb)
+    torch.cuda.synchronize()
+    rc, ro, rt, rr = O.bucket(idx, E)
+    np.testing.assert_array_equal(counts.cpu().numpy(), rc)
+    np.testing.assert_array_equal(offsets.cpu().numpy(), ro)
+    np.testing.assert_array_equal(pt.cpu().numpy(), rt)
+    np.testing.assert_array_equal(pr.cpu().numpy(), rr)
+    assert B.moe_get_device_error() == 0
