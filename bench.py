@@ -5,7 +5,7 @@
                     [--impl ours|reference]
 
 One bench step = `--tokens` (default 1000) batch-1 decode tokens, each a full
-pass of the layer (router GEMV, top-k, fused int4 gate/up SwiGLU, down +
+moe_layer_forward pass of the layer (router GEMV, top-k, fused int4 gate/up SwiGLU, down +
 weighted combine + gated shared expert) on its own seeded x, every expert
 read by indirection through the shuffled slot table of an all-resident HBM
 pool.  The step is captured once as a CUDA graph and replayed.  To keep the
@@ -13,8 +13,9 @@ weights from being served by the 126 MB L2, consecutive tokens rotate through
 R full copies of the layer (R chosen so the rotating working set is at least
 3x L2).
 
-Reported: tokens/s (whole job, all ranks), the experts phase's achieved HBM
-bandwidth on algorithmic bytes against the measured copy peak, the oracle's
+Reported: tokens/s (whole job, all ranks), the layer step's achieved HBM
+bandwidth on algorithmic bytes (active expert bytes over the event-timed
+duration of sampled layer calls) against the measured copy peak, the oracle's
 CPU throughput on a bounded sample, and an end-to-end number through the
 public C-ABI calls with pinned host buffers and copies inside the timed
 region.  Multi-GPU runs are independent replicas (the layer does not shard
@@ -44,7 +45,7 @@ from int4_routed_expert_06_b300 import synth  # noqa: E402
 METRIC = "routed-MoE layer tokens/s (decode, 512e top-10 int4); HBM GB/s vs peak"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6400.0
-KERNELS_PER_TOKEN = 4  # router, top-k, gate/up SwiGLU, down + combine
+KERNELS_PER_TOKEN = 3  # single-token path: router, gate/up SwiGLU (+ top-k), down + combine (+ top-k)
 
 
 def peaks():
@@ -165,7 +166,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="80b-dec", choices=["80b-dec", "35b-dec"])
     ap.add_argument("--tokens", type=int, default=1000, help="decode tokens per bench step")
-    ap.add_argument("--time-every", type=int, default=4, help="event-time the experts phase of every n-th token")
+    ap.add_argument("--time-every", type=int, default=8, help="event-time the layer call of every n-th token")
+    ap.add_argument("--replicas", type=int, default=0, help="layer copies to rotate through (0 = >= 3x L2)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -195,7 +197,7 @@ def main():
     per_token = synth.active_expert_bytes(shape)
     router_bytes = shape.n_experts * shape.hidden * 2 + shape.hidden * 2
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
-    R = max(1, math.ceil(3 * l2 / (per_token + router_bytes)))
+    R = args.replicas if args.replicas > 0 else max(1, math.ceil(3 * l2 / (per_token + router_bytes)))
     dl = B.DeviceLayer(shape, w, slots, replicas=R)
     T = args.tokens
     xs = synth.decode_xs(shape, T, device="cuda")
@@ -204,22 +206,15 @@ def main():
     k = shape.top_k
     nb = B.moe_layer_workspace_bytes(cfg, 1)
     ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
-    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
-    tw = torch.empty((T, k), dtype=torch.float32, device="cuda")
-    sg = torch.empty((T,), dtype=torch.float32, device="cuda")
     timed = list(range(0, T, args.time_every))
     ev = {j: (torch.cuda.Event(enable_timing=True, external=True),
               torch.cuda.Event(enable_timing=True, external=True)) for j in timed}
 
     def one_step():
         for j in range(T):
-            rep = dl.replicas[j % R]
-            B.moe_route(cfg, xs[j:j + 1], 1, rep["w_router"], rep["router_bias"], rep["w_shared_gate"],
-                        idx[j:j + 1], tw[j:j + 1], sg[j:j + 1], None, ws, nb)
             if j in ev:
                 ev[j][0].record()
-            B.moe_experts_forward(cfg, rep["struct"], xs[j:j + 1], 1, idx[j:j + 1], tw[j:j + 1],
-                                  sg[j:j + 1], ys[j:j + 1], None, ws, nb)
+            B.moe_layer_forward(cfg, dl.struct(j % R), xs[j:j + 1], 1, ys[j:j + 1], None, None, None, ws, nb)
             if j in ev:
                 ev[j][1].record()
 
@@ -251,7 +246,7 @@ def main():
         if dist:
             dist.barrier()
     ms = start.elapsed_time(end)
-    expert_us = [ev[j][0].elapsed_time(ev[j][1]) * 1e3 for j in timed]  # last replay
+    step_us = [ev[j][0].elapsed_time(ev[j][1]) * 1e3 for j in timed]  # last replay
     if B.moe_get_device_error(stream) != 0:
         raise RuntimeError("a kernel recorded a device error during the bench")
     ms_all = torch.tensor([ms], device="cuda")
@@ -290,9 +285,10 @@ def main():
             dist.destroy_process_group()
         return
 
-    # ---- roofline of the experts phase (gate/up SwiGLU + down/combine kernels)
+    # ---- roofline of the layer step (router, gate/up SwiGLU, down/combine
+    # kernels chained with programmatic dependent launch)
     peak, peak_kind = peaks()
-    mean_us = sum(expert_us) / len(expert_us)
+    mean_us = sum(step_us) / len(step_us)
     achieved = per_token / (mean_us * 1e-6) / 1e9
     step_gbs = per_token * T * args.steps / (ms / 1e3) / 1e9
     traffic = None
@@ -317,12 +313,14 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": workload_desc(shape), "tokens_per_step": T, "parallelism": f"replicas{world}",
                    "l2": f"inputs larger than L2: tokens rotate through {R} full layer copies "
-                         f"({R * dl.stride * dl.n_slots / 1e9:.1f} GB, >= 3x the {l2 / 1e6:.0f} MB L2)",
+                         f"({R * dl.stride * dl.n_slots / 1e9:.1f} GB; the weights {R} tokens touch are "
+                         f"{R * (per_token + router_bytes) / 1e6:.0f} MB vs the {l2 / 1e6:.0f} MB L2)",
                    "graph": "one CUDA graph per step (route + experts calls per token)"},
         "active_expert_bytes_per_token": per_token,
         "hbm": {"achieved_gbs_step": step_gbs, "frac_measured_step": step_gbs / peak,
                 "frac_nominal_8tbs_step": step_gbs / NOMINAL_HBM_GBS},
-        "roofline": {"kernel": "experts phase: gate/up SwiGLU + down/combine (2 kernels)", "bound": "hbm",
+        "roofline": {"kernel": "decode layer step: router + gate/up SwiGLU + down/combine kernels, PDL-chained",
+                     "bound": "hbm",
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "mean_us": mean_us,
                      "algorithmic_bytes_per_launch": per_token},

@@ -200,6 +200,8 @@ typedef struct slot_pool slot_pool;
 
 typedef struct {
     int64_t lookups, hits, misses, evictions, bytes_filled;
+    int64_t exposed_copy_ns; /* time compute streams spent waiting for fills
+                                (moe_pooled_layer_forward only) */
 } moe_pool_stats;
 
 moe_status slot_pool_create(const moe_config *cfg, int32_t n_layers, int32_t slots_per_layer,
@@ -229,6 +231,27 @@ moe_status slot_pool_layer(slot_pool *p, int32_t layer, const int32_t **table_de
 /* Copy of the host table row of `layer` into table_host [E]. */
 moe_status slot_pool_table_host(slot_pool *p, int32_t layer, int32_t *table_host);
 
+/* The resident part of one layer: router, optional router bias, shared-gate
+ * vector and shared-expert blob (device pointers, as in moe_layer). */
+typedef struct {
+    const void *w_router;
+    const float *router_bias;
+    const void *w_shared_gate;
+    const void *shared_blob;
+} moe_resident_weights;
+
+/* One layer of a pooled stack, end to end: route x on `stream`, read the
+ * top-k ids back to the host (the one synchronisation of `stream`), apply the
+ * pool policy, fill the misses on the pool's side stream, make `stream` wait
+ * for the fills, then run the experts from the pool.  T tokens; their
+ * distinct experts must fit the layer's slots (MOE_ERR_POOL_EXHAUSTED
+ * otherwise).  x, y, y_f32 (nullable), topk_idx_out (nullable) and workspace
+ * (moe_layer_workspace_bytes) are device pointers. */
+moe_status moe_pooled_layer_forward(const moe_config *cfg, slot_pool *p, int32_t layer,
+                                    const moe_resident_weights *w, const void *x, int32_t T, void *y,
+                                    float *y_f32, int32_t *topk_idx_out, void *workspace,
+                                    size_t ws_bytes, cudaStream_t stream);
+
 moe_status slot_pool_stats(slot_pool *p, moe_pool_stats *out);
 void slot_pool_destroy(slot_pool *p);
 
@@ -244,6 +267,13 @@ const char *moe_last_error_message(void);
 
 /* Library version string. */
 const char *moe_version(void);
+
+/* Kernel selection for single-token calls, process-wide: 0 (default) uses the
+ * single-token kernels (bulk-copy staged, PDL-chained) where the shape allows,
+ * 1 forces the generic kernels everywhere.  The two compute the same function
+ * (the pages' practice of checking fast against scalar kernels); tests compare
+ * both against the CPU oracle.  MOE_ERR_INVALID_ARG for other values. */
+moe_status moe_set_kernel_path(int32_t path);
 
 #ifdef __cplusplus
 }

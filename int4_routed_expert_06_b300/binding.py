@@ -63,7 +63,13 @@ class moe_layer(C.Structure):
 
 
 class moe_pool_stats(C.Structure):
-    _fields_ = [(n, C.c_int64) for n in ("lookups", "hits", "misses", "evictions", "bytes_filled")]
+    _fields_ = [(n, C.c_int64) for n in ("lookups", "hits", "misses", "evictions", "bytes_filled",
+                                         "exposed_copy_ns")]
+
+
+class moe_resident_weights(C.Structure):
+    _fields_ = [("w_router", C.c_void_p), ("router_bias", C.c_void_p), ("w_shared_gate", C.c_void_p),
+                ("shared_blob", C.c_void_p)]
 
 
 # ------------------------------------------------------------------ loading
@@ -89,10 +95,13 @@ _SIGS = {
     "slot_pool_layer": (_I, [_P, _I, _CP(_P), _CP(_P)]),
     "slot_pool_table_host": (_I, [_P, _I, _P]),
     "slot_pool_stats": (_I, [_P, _CP(moe_pool_stats)]),
+    "moe_pooled_layer_forward": (_I, [_CP(moe_config), _P, _I, _CP(moe_resident_weights), _P, _I, _P, _P, _P,
+                                      _P, _Z, _P]),
     "slot_pool_destroy": (None, [_P]),
     "moe_get_device_error": (_I, [_P]),
     "moe_last_error_message": (C.c_char_p, []),
     "moe_version": (C.c_char_p, []),
+    "moe_set_kernel_path": (_I, [_I]),
 }
 
 
@@ -123,7 +132,7 @@ def header_functions() -> list:
 def _check(st: int, what: str):
     if st != MOE_OK:
         msg = lib().moe_last_error_message().decode(errors="replace")
-        raise MoEError(st, f"{what}: {msg}")
+        raise MoEError(st, msg if msg.startswith(what) else f"{what}: {msg}")
 
 
 def _ptr(t) -> Optional[int]:
@@ -249,6 +258,13 @@ def slot_pool_stats(pool: int) -> dict:
     return {n: getattr(s, n) for n, _ in moe_pool_stats._fields_}
 
 
+def moe_pooled_layer_forward(cfg, pool: int, layer: int, weights: moe_resident_weights, x, T, y, y_f32,
+                             topk_idx_out, workspace, ws_bytes, stream=None):
+    _check(lib().moe_pooled_layer_forward(C.byref(cfg), pool, layer, C.byref(weights), _ptr(x), T, _ptr(y),
+                                          _ptr(y_f32), _ptr(topk_idx_out), _ptr(workspace), ws_bytes,
+                                          _stream(stream)), "moe_pooled_layer_forward")
+
+
 def slot_pool_destroy(pool: int) -> None:
     lib().slot_pool_destroy(pool)
 
@@ -264,6 +280,10 @@ def moe_last_error_message() -> str:
 
 def moe_version() -> str:
     return lib().moe_version().decode()
+
+
+def moe_set_kernel_path(path: int) -> None:
+    _check(lib().moe_set_kernel_path(path), "moe_set_kernel_path")
 
 
 # ------------------------------------------------------------------ marshalling helpers

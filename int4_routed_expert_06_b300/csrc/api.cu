@@ -10,6 +10,9 @@
 namespace moe {
 
 static thread_local char t_msg[512] = "";
+static int g_kernel_path = 0;
+
+int kernel_path() { return g_kernel_path; }
 
 moe_status fail(moe_status st, const char *fmt, ...)
 {
@@ -109,7 +112,15 @@ extern "C" {
 
 const char *moe_last_error_message(void) { return t_msg; }
 
-const char *moe_version(void) { return "moe_int4 0.1 (sm_103a)"; }
+const char *moe_version(void) { return "moe_int4 0.2 (sm_103a)"; }
+
+moe_status moe_set_kernel_path(int32_t path)
+{
+    if (path != 0 && path != 1)
+        return fail(MOE_ERR_INVALID_ARG, "moe_set_kernel_path: path %d must be 0 or 1", path);
+    g_kernel_path = path;
+    return MOE_OK;
+}
 
 moe_status moe_blob_layout_get(const moe_config *cfg, int32_t inter, moe_blob_layout *out)
 {
@@ -223,8 +234,12 @@ moe_status moe_route(const moe_config *cfg, const void *x, int32_t T, const void
             return fail(MOE_ERR_OOM, "moe_route: workspace needs %zu bytes (256-byte aligned), got %zu", w.total, ws_bytes);
         logits = reinterpret_cast<float *>(static_cast<char *>(workspace) + w.logits);
     }
-    cudaError_t e = launch_router(s, x, T, w_router, router_bias, s.Is > 0 ? w_shared_gate : nullptr, logits,
-                                  shared_gate_logit, stream);
+    cudaError_t e;
+    if (T == 1 && fast::eligible(s))
+        e = fast::launch_router_fast(s, x, w_router, router_bias, w_shared_gate, logits, shared_gate_logit, stream);
+    else
+        e = launch_router(s, x, T, w_router, router_bias, s.Is > 0 ? w_shared_gate : nullptr, logits,
+                          shared_gate_logit, stream);
     if (e != cudaSuccess)
         return cuda_check(e, "moe_route: router");
     e = launch_topk(s, logits, T, topk_idx, topk_w, stream);
@@ -357,6 +372,10 @@ moe_status moe_experts_forward(const moe_config *cfg, const moe_layer *L, const 
         return fail(MOE_ERR_OOM, "moe_experts_forward: workspace needs %zu bytes (256-byte aligned), got %zu",
                     w.total, ws_bytes);
     float *a = reinterpret_cast<float *>(static_cast<char *>(workspace) + w.a);
+    if (T == 1 && fast::eligible(s)) {
+        fast::Routing R{nullptr, topk_idx, topk_w, nullptr, nullptr, shared_gate_logit};
+        return cuda_check(fast::launch_experts_fast(s, x, src, R, a, y, y_f32, stream), "moe_experts_forward");
+    }
     const int n_act = s.k + (s.Is > 0 ? 1 : 0);
     cudaError_t e = launch_gateup(s, x, T, s.k, n_act, topk_idx, src, a, imax_of(s), stream);
     if (e != cudaSuccess)
@@ -388,6 +407,23 @@ moe_status moe_layer_forward(const moe_config *cfg, const moe_layer *L, const vo
     int32_t *idx = topk_idx_out ? topk_idx_out : reinterpret_cast<int32_t *>(ws + w.idx);
     float *tw = topk_w_out ? topk_w_out : reinterpret_cast<float *>(ws + w.w);
     float *sg = s.Is > 0 ? reinterpret_cast<float *>(ws + w.sg) : nullptr;
+    if (T == 1 && fast::eligible(s)) {
+        if (!aligned(x, 16) || !L->w_router || !aligned(L->w_router, 16) || !L->w_shared_gate ||
+            !aligned(L->w_shared_gate, 16) || !y)
+            return fail(MOE_ERR_INVALID_ARG, "moe_layer_forward: x, y, w_router and w_shared_gate must be non-NULL "
+                                             "and 16-byte aligned");
+        ExpertSrc src;
+        if ((st = make_src(cfg, s, L, &src, "moe_layer_forward")) != MOE_OK)
+            return st;
+        float *logits = reinterpret_cast<float *>(ws + w.logits);
+        cudaError_t e = fast::launch_router_fast(s, x, L->w_router, L->router_bias, L->w_shared_gate, logits, sg,
+                                                 stream);
+        if (e != cudaSuccess)
+            return cuda_check(e, "moe_layer_forward: router");
+        fast::Routing R{logits, nullptr, nullptr, idx, tw, sg};
+        float *a = reinterpret_cast<float *>(ws + w.a);
+        return cuda_check(fast::launch_experts_fast(s, x, src, R, a, y, y_f32, stream), "moe_layer_forward: experts");
+    }
     st = moe_route(cfg, x, T, L->w_router, L->router_bias, s.Is > 0 ? L->w_shared_gate : nullptr, idx, tw, sg,
                    reinterpret_cast<float *>(ws + w.logits), nullptr, 0, stream);
     if (st != MOE_OK)

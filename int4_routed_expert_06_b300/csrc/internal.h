@@ -42,4 +42,27 @@ cudaError_t launch_bucket(const Shape &s, const int32_t *idx, int T, int32_t *co
                           int32_t *chunk_hist, cudaStream_t st);
 int bucket_chunks(int pairs);
 
+// 0 = use the single-token fast kernels where eligible, 1 = generic kernels only.
+int kernel_path();
+
+namespace fast {
+// Routing of one token for the fast expert kernels: either top-k from logits
+// (every CTA recomputes it) or given idx / w.
+struct Routing {
+    const float *logits;     // [E] or NULL when idx/w are given
+    const int32_t *idx;      // [k] given, or NULL
+    const float *w;          // [k] given, or NULL
+    int32_t *idx_out;        // [k] written by CTA 0 of gate/up (logits mode), or NULL
+    float *w_out;            // [k]
+    const float *sg_logit;   // [1] shared-gate logit
+};
+// Shapes the single-token kernels handle (bf16 activations, H in {1024, 2048,
+// 4096}, a shared expert, 16-byte scale rows, shares that fit shared memory).
+bool eligible(const Shape &s);
+cudaError_t launch_router_fast(const Shape &s, const void *x, const void *w_router, const float *bias,
+                               const void *w_sg, float *logits, float *sg, cudaStream_t st);
+cudaError_t launch_experts_fast(const Shape &s, const void *x, const ExpertSrc &src, const Routing &R, float *a,
+                                void *y, float *y32, cudaStream_t st);
+} // namespace fast
+
 } // namespace moe

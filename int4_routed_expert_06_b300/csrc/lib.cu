@@ -2,5 +2,6 @@
 // __device__ variable shared by every kernel, so all sources compile together.
 #include "api.cu"
 #include "kernels_decode.cu"
+#include "kernels_fast.cu"
 #include "bucket.cu"
 #include "slot_pool.cu"

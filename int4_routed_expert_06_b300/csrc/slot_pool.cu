@@ -58,6 +58,13 @@ struct slot_pool {
     int32_t *table_dev = nullptr;
     moe_pool_stats st{};
     std::mutex mu;
+    // moe_pooled_layer_forward: pinned readback of the routed ids, scratch
+    // lists, and events that time the compute stream's wait for fills.
+    int32_t *pinned_ids = nullptr;
+    size_t pinned_cap = 0;
+    std::vector<int32_t> tmp_slots, tmp_miss;
+    cudaEvent_t fill_done = nullptr, wait_begin = nullptr, wait_end = nullptr;
+    bool pending_exposure = false;
 };
 
 extern "C" moe_status slot_pool_create(const moe_config *cfg, int32_t n_layers, int32_t slots_per_layer,
@@ -287,21 +294,139 @@ extern "C" moe_status slot_pool_table_host(slot_pool *p, int32_t layer, int32_t 
     return MOE_OK;
 }
 
+// Add the last pooled forward's fill wait to the stats once it has finished.
+static void harvest_exposure(slot_pool *p)
+{
+    if (!p->pending_exposure)
+        return;
+    float ms = 0.f;
+    if (cudaEventSynchronize(p->wait_end) == cudaSuccess &&
+        cudaEventElapsedTime(&ms, p->wait_begin, p->wait_end) == cudaSuccess)
+        p->st.exposed_copy_ns += (int64_t)(ms * 1.0e6);
+    p->pending_exposure = false;
+}
+
 extern "C" moe_status slot_pool_stats(slot_pool *p, moe_pool_stats *out)
 {
     using namespace moe;
     if (!p || !out)
         return fail(MOE_ERR_INVALID_ARG, "slot_pool_stats: NULL argument");
     std::lock_guard<std::mutex> g(p->mu);
+    harvest_exposure(p);
     *out = p->st;
     return MOE_OK;
+}
+
+extern "C" moe_status moe_pooled_layer_forward(const moe_config *cfg, slot_pool *p, int32_t layer,
+                                               const moe_resident_weights *w, const void *x, int32_t T, void *y,
+                                               float *y_f32, int32_t *topk_idx_out, void *workspace,
+                                               size_t ws_bytes, cudaStream_t stream)
+{
+    using namespace moe;
+    Shape s;
+    moe_status st = check_config(cfg, &s);
+    if (st != MOE_OK)
+        return st;
+    if (!p || !w || !w->w_router)
+        return fail(MOE_ERR_INVALID_ARG, "moe_pooled_layer_forward: NULL pool, weights or router");
+    if (s.H != p->s.H || s.E != p->s.E || s.k != p->s.k || s.I != p->s.I || s.G != p->s.G ||
+        s.qscale != p->s.qscale)
+        return fail(MOE_ERR_INVALID_ARG, "moe_pooled_layer_forward: config differs from the pool's");
+    if (layer < 0 || layer >= p->L)
+        return fail(MOE_ERR_INVALID_ARG, "moe_pooled_layer_forward: layer %d out of range", layer);
+    if (T < 0 || T > 65535)
+        return fail(MOE_ERR_INVALID_ARG, "moe_pooled_layer_forward: T %d out of range", T);
+    if (T == 0)
+        return MOE_OK;
+    const Ws ws = layer_ws(s, T);
+    if (!workspace || ws_bytes < ws.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return fail(MOE_ERR_OOM, "moe_pooled_layer_forward: workspace needs %zu bytes (256-byte aligned), got %zu",
+                    ws.total, ws_bytes);
+    char *wsp = static_cast<char *>(workspace);
+    int32_t *idx = topk_idx_out ? topk_idx_out : reinterpret_cast<int32_t *>(wsp + ws.idx);
+    float *tw = reinterpret_cast<float *>(wsp + ws.w);
+    float *sg = s.Is > 0 ? reinterpret_cast<float *>(wsp + ws.sg) : nullptr;
+    float *logits = reinterpret_cast<float *>(wsp + ws.logits);
+    st = moe_route(cfg, x, T, w->w_router, w->router_bias, s.Is > 0 ? w->w_shared_gate : nullptr, idx, tw, sg,
+                   logits, nullptr, 0, stream);
+    if (st != MOE_OK)
+        return st;
+
+    const size_t n_ids = (size_t)T * s.k;
+    {
+        std::lock_guard<std::mutex> g(p->mu);
+        moe_status ts = ensure_table_dev(p);
+        if (ts != MOE_OK)
+            return ts;
+        cudaError_t e = cudaSuccess;
+        if (!p->fill_done) {
+            e = cudaEventCreateWithFlags(&p->fill_done, cudaEventDisableTiming);
+            if (e == cudaSuccess)
+                e = cudaEventCreate(&p->wait_begin);
+            if (e == cudaSuccess)
+                e = cudaEventCreate(&p->wait_end);
+        }
+        if (e == cudaSuccess && n_ids > p->pinned_cap) {
+            if (p->pinned_ids)
+                cudaFreeHost(p->pinned_ids);
+            p->pinned_ids = nullptr;
+            p->pinned_cap = 0;
+            e = cudaHostAlloc(reinterpret_cast<void **>(&p->pinned_ids), n_ids * sizeof(int32_t),
+                              cudaHostAllocDefault);
+            if (e == cudaSuccess)
+                p->pinned_cap = n_ids;
+        }
+        if (e != cudaSuccess)
+            return cuda_check(e, "moe_pooled_layer_forward: host buffers");
+        harvest_exposure(p);
+    }
+    cudaError_t e = cudaMemcpyAsync(p->pinned_ids, idx, n_ids * sizeof(int32_t), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess)
+        return cuda_check(e, "moe_pooled_layer_forward: routing readback");
+
+    p->tmp_slots.resize(n_ids);
+    p->tmp_miss.resize(n_ids);
+    int32_t n_miss = 0;
+    st = slot_pool_lookup(p, layer, p->pinned_ids, (int32_t)n_ids, p->tmp_slots.data(), p->tmp_miss.data(),
+                          &n_miss);
+    if (st != MOE_OK)
+        return st;
+    if (n_miss > 0) {
+        st = slot_pool_fill(p, layer, p->tmp_miss.data(), n_miss, p->fill_done);
+        if (st != MOE_OK)
+            return st;
+        e = cudaEventRecord(p->wait_begin, stream);
+        if (e == cudaSuccess)
+            e = cudaStreamWaitEvent(stream, p->fill_done, 0);
+        if (e == cudaSuccess)
+            e = cudaEventRecord(p->wait_end, stream);
+        if (e != cudaSuccess)
+            return cuda_check(e, "moe_pooled_layer_forward: fill ordering");
+        std::lock_guard<std::mutex> g(p->mu);
+        p->pending_exposure = true;
+    }
+    moe_layer L{w->w_router, w->router_bias, w->w_shared_gate, w->shared_blob,
+                p->pool + (size_t)layer * p->S * p->stride, p->stride, p->table_dev + (size_t)layer * s.E, p->S};
+    return moe_experts_forward(cfg, &L, x, T, idx, tw, sg, y, y_f32, workspace, ws_bytes, stream);
 }
 
 extern "C" void slot_pool_destroy(slot_pool *p)
 {
     if (!p)
         return;
+    if (p->pending_exposure && p->wait_end)
+        cudaEventSynchronize(p->wait_end);
     if (p->table_dev)
         cudaFree(p->table_dev);
+    if (p->pinned_ids)
+        cudaFreeHost(p->pinned_ids);
+    if (p->fill_done)
+        cudaEventDestroy(p->fill_done);
+    if (p->wait_begin)
+        cudaEventDestroy(p->wait_begin);
+    if (p->wait_end)
+        cudaEventDestroy(p->wait_end);
     delete p;
 }

@@ -1,0 +1,94 @@
+"""A stack of MoE layers served from a bounded HBM expert pool.
+
+Memory plumbing around the C-ABI: a pinned host backing store holding every
+layer's expert blobs at a fixed stride, the device pool buffer, the resident
+part of each layer (router, shared gate, shared expert) and the side stream
+fills run on.  Each layer step is one ``moe_pooled_layer_forward`` call; the
+routing, the LFU+recency policy, the fills and the expert kernels all run in
+the library.
+"""
+from __future__ import annotations
+
+from typing import Callable, Dict, List
+
+import torch
+
+from . import binding as B
+
+
+class PooledStack:
+    def __init__(self, shape, n_layers: int, slots_per_layer: int,
+                 layer_weights: Callable[[int], Dict[str, torch.Tensor]], device: str = "cuda"):
+        self.shape, self.cfg = shape, B.config_for(shape)
+        self.L, self.S, self.E = n_layers, slots_per_layer, shape.n_experts
+        lay = B.moe_blob_layout_get(self.cfg, shape.inter)
+        self.blob_bytes = lay.bytes
+        self.stride = (lay.bytes + 255) // 256 * 256
+        self.backing = torch.empty((n_layers, self.E, self.stride), dtype=torch.uint8, pin_memory=True)
+        self.pool = torch.empty((n_layers * slots_per_layer * self.stride,), dtype=torch.uint8, device=device)
+        ident = torch.arange(self.E, dtype=torch.int32)
+        self.resident: List[dict] = []
+        for l in range(n_layers):
+            w = layer_weights(l)
+            blobs = B.pack_blobs(self.cfg, shape.inter, w, ident, self.E, self.stride)
+            self.backing[l].copy_(blobs)
+            del blobs
+            sh_lay = B.moe_blob_layout_get(self.cfg, shape.shared_inter)
+            sh_stride = (sh_lay.bytes + 255) // 256 * 256
+            shared = B.pack_blobs(self.cfg, shape.shared_inter, w, torch.zeros(1, dtype=torch.int32), 1,
+                                  sh_stride, prefix="shared_")
+            r = {"w_router": w["w_router"].contiguous(), "w_shared_gate": w["w_shared_gate"].contiguous(),
+                 "router_bias": w.get("router_bias"), "shared": shared}
+            r["struct"] = B.moe_resident_weights(
+                r["w_router"].data_ptr(), r["router_bias"].data_ptr() if r["router_bias"] is not None else None,
+                r["w_shared_gate"].data_ptr(), shared.data_ptr())
+            self.resident.append(r)
+        self.side = torch.cuda.Stream()
+        self.handle = B.slot_pool_create(self.cfg, n_layers, slots_per_layer, self.pool, self.pool.numel(),
+                                         self.backing, self.stride, self.side)
+        self.ws_bytes = 0
+        self.ws = None
+
+    def workspace(self, T: int) -> torch.Tensor:
+        nb = B.moe_layer_workspace_bytes(self.cfg, T)
+        if self.ws is None or nb > self.ws_bytes:
+            self.ws = torch.empty(max(nb, 256), dtype=torch.uint8, device=self.pool.device)
+            self.ws_bytes = nb
+        return self.ws
+
+    def layer_forward(self, l: int, x: torch.Tensor, y: torch.Tensor, y32=None, idx_out=None, stream=None):
+        T = x.shape[0]
+        ws = self.workspace(T)
+        B.moe_pooled_layer_forward(self.cfg, self.handle, l, self.resident[l]["struct"], x, T, y, y32, idx_out,
+                                   ws, self.ws_bytes, stream)
+
+    def table_device(self, l: int) -> torch.Tensor:
+        """Copy of layer l's device table row ([E] int32)."""
+        ptr, _ = B.slot_pool_layer(self.handle, l)
+        return torch.as_tensor(_DeviceArray(ptr, self.E), device=self.pool.device).clone()
+
+    def slot_bytes(self, l: int, slot: int) -> torch.Tensor:
+        base = (l * self.S + slot) * self.stride
+        return self.pool[base:base + self.blob_bytes]
+
+    def stats(self) -> dict:
+        return B.slot_pool_stats(self.handle)
+
+    def close(self):
+        if self.handle:
+            torch.cuda.synchronize()
+            B.slot_pool_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class _DeviceArray:
+    """An int32 device array at a raw address, viewable by torch.as_tensor."""
+
+    def __init__(self, ptr: int, n: int):
+        self.__cuda_array_interface__ = {"shape": (n,), "typestr": "<i4", "data": (ptr, False), "version": 3}

@@ -72,20 +72,33 @@ def test_topk_ties_and_k_equals_e_on_device():
     idx = torch.empty((2, 8), dtype=torch.int32, device="cuda")
     tw = torch.empty((2, 8), device="cuda")
     sg = torch.empty(2, device="cuda")
-    B.moe_route(cfg, x, 2, wr, None, wsg, idx, tw, sg)
+    lg = torch.empty((2, E), device="cuda")
+    B.moe_route(cfg, x, 2, wr, None, wsg, idx, tw, sg, lg)
     torch.cuda.synchronize()
     assert idx[0].tolist() == [1, 2, 4, 7, 3, 0, 6, 5]
     ref_idx, ref_w = O.topk(wr[:, 0].double().cpu().numpy(), 8)
     np.testing.assert_allclose(tw[0].cpu().numpy(), ref_w, rtol=1e-6)
     cfg.top_k = 1
-    B.moe_route(cfg, x, 2, wr, None, wsg, idx, tw, sg)
+    B.moe_route(cfg, x, 2, wr, None, wsg, idx, tw, sg, lg)
     torch.cuda.synchronize()
     assert idx[0, 0].item() == 1 and tw[0, 0].item() == 1.0
 
 
+@pytest.fixture
+def kernel_path():
+    """Select the single-token fast kernels (0) or the generic ones (1)."""
+    def set_path(p):
+        B.moe_set_kernel_path(p)
+    yield set_path
+    B.moe_set_kernel_path(0)
+
+
+@pytest.mark.parametrize("path", [0, 1])
 @pytest.mark.parametrize("name", NAMES)
-def test_layer_decode_parity(name):
-    """T = 1 decode steps, each its own call (the bench's configuration)."""
+def test_layer_decode_parity(name, path, kernel_path):
+    """T = 1 decode steps, each its own call (the bench's configuration), on
+    the fast single-token kernels and on the generic ones."""
+    kernel_path(path)
     shape, w, L = layer_of(name)
     dl = device_layer(name)
     xs = _xs(name, 6)
@@ -124,13 +137,60 @@ def test_expert_forward_parity(name):
         ex = B.expert_struct(w, e)
         y = torch.empty((T, shape.hidden), dtype=synth.torch_dtype(shape.act), device="cuda")
         y32 = torch.empty((T, shape.hidden), device="cuda")
-        nb = B.moe_expert_workspace_bytes(dl_cfg := B.config_for(shape), T)
-        ws = workspace(nb)
-        B.moe_expert_forward(dl_cfg, ex, shape.inter, x, T, y, y32, ws, nb)
+        cfg = B.config_for(shape)
+        nb = B.moe_expert_workspace_bytes(cfg, T)
+        B.moe_expert_forward(cfg, ex, shape.inter, x, T, y, y32, workspace(nb), nb)
         torch.cuda.synchronize()
         view = O.ExpertView(w, e)
         ref = np.stack([O.expert(view, shape.group, x[t]) for t in range(T)])
         assert_close(y32.cpu().numpy(), ref, shape.act, f"expert {e}")
+
+
+@pytest.mark.parametrize("name", ["35b-dec", "80b-dec"])
+def test_route_then_experts_parity(name):
+    """moe_route followed by moe_experts_forward (routing passed in) at T = 1."""
+    shape, w, L = layer_of(name)
+    dl = device_layer(name)
+    xs = _xs(name, 4)
+    rep = dl.replicas[0]
+    nb = B.moe_layer_workspace_bytes(dl.cfg, 1)
+    ws = workspace(nb)
+    for s in range(4):
+        x = xs[s:s + 1]
+        idx = torch.empty((1, shape.top_k), dtype=torch.int32, device="cuda")
+        tw = torch.empty((1, shape.top_k), device="cuda")
+        sg = torch.empty((1,), device="cuda")
+        y = torch.empty((1, shape.hidden), dtype=torch.bfloat16, device="cuda")
+        y32 = torch.empty((1, shape.hidden), device="cuda")
+        B.moe_route(dl.cfg, x, 1, rep["w_router"], rep["router_bias"], rep["w_shared_gate"], idx, tw, sg, None,
+                    ws, nb)
+        B.moe_experts_forward(dl.cfg, rep["struct"], x, 1, idx, tw, sg, y, y32, ws, nb)
+        torch.cuda.synchronize()
+        assert B.moe_get_device_error() == 0
+        ref = L.forward(x)
+        if near_tie_tokens(ref["logits"], shape.top_k)[0]:
+            continue
+        np.testing.assert_array_equal(idx.cpu().numpy(), ref["idx"])
+        assert_close(y32.cpu().numpy(), ref["y"], shape.act, f"{name} step {s}")
+
+
+def test_fast_and_generic_kernels_agree():
+    """The single-token kernels and the generic ones compute the same layer
+    (different summation order, so within a few fp32 ulps of the output scale)."""
+    name = "80b-dec"
+    dl = device_layer(name)
+    xs = _xs(name, 3)
+    try:
+        for s in range(3):
+            B.moe_set_kernel_path(0)
+            a = layer_forward(dl, xs[s:s + 1])
+            B.moe_set_kernel_path(1)
+            b = layer_forward(dl, xs[s:s + 1])
+            assert torch.equal(a[2], b[2])                      # same routing
+            d = (a[1] - b[1]).abs().max().item()
+            assert d <= 1e-5 * max(1.0, b[1].abs().max().item()), d
+    finally:
+        B.moe_set_kernel_path(0)
 
 
 def test_pool_placement_never_changes_the_result():
