@@ -178,6 +178,25 @@ moe_status moe_layer_forward(const moe_config *cfg, const moe_layer *layer, cons
                              float *topk_w_out, void *workspace, size_t ws_bytes,
                              cudaStream_t stream);
 
+/* moe_layer_forward without a caller workspace, for callers that cannot
+ * allocate device memory where they run the layer (an engine plugin whose
+ * host owns all device memory, a latency-critical loop that must not take
+ * cudaMalloc's implicit synchronisation).  The Swiftlet pages have no
+ * counterpart; this is an interface convenience.
+ * Scratch is a 4 MiB array built into the library's device image, held by
+ * every GPU that loads the library until the process exits; T is limited to
+ * what fits (moe_layer_workspace_bytes(cfg, T) <= 4 MiB, about T <= 160 for
+ * the 80B shape), larger T returns MOE_ERR_OOM.  Nothing is allocated: no
+ * cudaMalloc, cudaFree or allocating library call.  The first call on each
+ * device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.  All
+ * calls on a device share the one array and it keeps the last call's
+ * contents; calls whose GPU work overlaps race on it, so order them (one
+ * stream, or events).  Other arguments and behaviour as moe_layer_forward. */
+moe_status moe_layer_forward_noalloc(const moe_config *cfg, const moe_layer *layer, const void *x,
+                                     int32_t T, void *y, float *y_f32, int32_t *topk_idx_out,
+                                     float *topk_w_out, cudaStream_t stream);
+
 /* ------------------------------------------------------------------ pool */
 
 /* A bounded HBM pool of expert slots for n_layers layers, filled on demand

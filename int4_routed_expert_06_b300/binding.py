@@ -89,6 +89,7 @@ _SIGS = {
     "moe_expert_forward": (_I, [_CP(moe_config), _CP(moe_expert), _I, _P, _I, _P, _P, _P, _Z, _P]),
     "moe_experts_forward": (_I, [_CP(moe_config), _CP(moe_layer), _P, _I, _P, _P, _P, _P, _P, _P, _Z, _P]),
     "moe_layer_forward": (_I, [_CP(moe_config), _CP(moe_layer), _P, _I, _P, _P, _P, _P, _P, _Z, _P]),
+    "moe_layer_forward_noalloc": (_I, [_CP(moe_config), _CP(moe_layer), _P, _I, _P, _P, _P, _P, _P]),
     "slot_pool_create": (_I, [_CP(moe_config), _I, _I, _P, _Z, _P, _Z, _P, _CP(_P)]),
     "slot_pool_lookup": (_I, [_P, _I, _P, _I, _P, _P, _CP(_I)]),
     "slot_pool_fill": (_I, [_P, _I, _P, _I, _P]),
@@ -210,6 +211,14 @@ def moe_layer_forward(cfg, layer: moe_layer, x, T, y, y_f32=None, topk_idx_out=N
     _check(lib().moe_layer_forward(C.byref(cfg), C.byref(layer), _ptr(x), T, _ptr(y), _ptr(y_f32),
                                    _ptr(topk_idx_out), _ptr(topk_w_out), _ptr(workspace), ws_bytes,
                                    _stream(stream)), "moe_layer_forward")
+
+
+def moe_layer_forward_noalloc(cfg, layer: moe_layer, x, T, y, y_f32=None, topk_idx_out=None, topk_w_out=None,
+                              stream=None):
+    """moe_layer_forward with the library's built-in scratch (no workspace argument)."""
+    _check(lib().moe_layer_forward_noalloc(C.byref(cfg), C.byref(layer), _ptr(x), T, _ptr(y), _ptr(y_f32),
+                                           _ptr(topk_idx_out), _ptr(topk_w_out), _stream(stream)),
+           "moe_layer_forward_noalloc")
 
 
 def slot_pool_create(cfg, n_layers, slots_per_layer, pool_dev, pool_bytes, backing_host, expert_stride,

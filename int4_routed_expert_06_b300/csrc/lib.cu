@@ -5,3 +5,4 @@
 #include "kernels_fast.cu"
 #include "bucket.cu"
 #include "slot_pool.cu"
+#include "noalloc.cu"
