@@ -36,7 +36,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxSeg = 4;          // gate/up segments per CTA (1 shared + up to 3 routed)
 constexpr int kMaxAct = 17;         // top_k <= 16 plus the shared expert
-constexpr unsigned kSpinLimit = 1u << 22;
+constexpr uint64_t kWaitNs = 200ull * 1000 * 1000; // 0.2 s bound on any barrier wait
 
 // ------------------------------------------------------------ PTX helpers
 
@@ -83,15 +83,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
-// Bounded wait for phase 0 of a single-use barrier; false (and the error word
-// set to MOE_ERR_TIMEOUT) if it never completes.
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase 0 of a single-use barrier, for at most kWaitNs of wall
+// time (try_wait may suspend between polls, so the bound is on time, not
+// on polls); false, with MOE_ERR_TIMEOUT recorded, if it never completes.
 __device__ __forceinline__ bool mbar_wait0(uint64_t *bar)
 {
-    for (unsigned it = 0; it < kSpinLimit; ++it)
-        if (mbar_try_wait(bar, 0))
-            return true;
-    record_error(MOE_ERR_TIMEOUT);
-    return false;
+    if (mbar_try_wait(bar, 0))
+        return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, 0))
+                return true;
+        if (global_ns() - t0 > kWaitNs) {
+            record_error(MOE_ERR_TIMEOUT);
+            return false;
+        }
+    }
 }
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -367,10 +382,11 @@ struct Seg {
 // H = 1024 * NXC; TS = scale/bias type.
 //
 // Warp 0 waits for the router (griddepcontrol.wait), selects the top k, and
-// issues the routed rows' copies (lane s handles segment s); meanwhile the
-// other warps already compute the shared expert's rows, whose copies were
-// issued before the wait.  Every segment barrier is armed exactly once, with
-// zero bytes when the expert has no slot, so no consumer can wait forever.
+// issues the routed rows' copies (lane s handles segment s); then all warps
+// compute, the shared expert's rows first (their copies were issued before
+// the wait), the routed rows as they land.  Every segment barrier is armed
+// exactly once, with zero bytes when the expert has no slot, so no consumer
+// can wait forever.
 template <int NXC, typename TS>
 __global__ void __launch_bounds__(kThreads, 1) gateup_fast_kernel(GateUpArgs A)
 {
@@ -460,7 +476,6 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_fast_kernel(GateUpArgs A)
 
     if (warp == 0) {
         pdl_wait();
-        pdl_trigger();
         load_routing(A.R, A.E, k, lane, s_idx, s_w, cand_v, cand_e, c == 0);
         if (lane < nseg && seg[lane].i != k) {
             const char *b = active_base(A.src, s_idx, k, seg[lane].i);
@@ -471,6 +486,10 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_fast_kernel(GateUpArgs A)
                 mbar_arrive_expect_tx(&bars[lane], 0);
         }
     }
+    // The routing is settled and every routed copy is in flight: the shared
+    // rows (already landed) are computed while the routed rows arrive.
+    __syncthreads();
+    pdl_trigger();
 
     int seg_start[kMaxSeg + 1];
     seg_start[0] = 0;
@@ -478,17 +497,11 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_fast_kernel(GateUpArgs A)
         seg_start[s + 1] = seg_start[s] + (s < nseg ? seg[s].n : 0);
     const int total = seg_start[nseg];
     int waited = -1;
-    bool joined = (warp == 0);
     for (int rho = warp; rho < total; rho += kWarps) {
         int s = 0;
         while (rho >= seg_start[s + 1])
             ++s;
         const Seg &g = seg[s];
-        if (!joined && g.i != k) { // first routed row of this warp: join the dependency
-            pdl_wait();
-            pdl_trigger();
-            joined = true;
-        }
         if (waited < s) {
             if (!mbar_wait0(&bars[s]))
                 return;
@@ -524,10 +537,6 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_fast_kernel(GateUpArgs A)
         if (lane == 0)
             *dst = gv * sigmoid_f(gv) * uv;
     }
-    if (!joined) {
-        pdl_wait();
-        pdl_trigger();
-    }
 }
 
 // ------------------------------------------------------------ down + combine
@@ -556,6 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) down_fast_kernel(DownArgs A)
     __shared__ int s_idx[kMaxAct];
     __shared__ float s_w[kMaxAct + 1];
     __shared__ const char *s_base[kMaxAct];
+    __shared__ uint32_t s_eoff[kMaxAct];
     __shared__ float cand_v[32];
     __shared__ int cand_e[32];
 
@@ -578,13 +588,17 @@ __global__ void __launch_bounds__(kThreads, 1) down_fast_kernel(DownArgs A)
     const uint32_t wbytes = exp_off(n_act);
 
     if (warp == 0) {
+        float sgl = 0.f;
         if (lane == 0) {
             mbar_init(&bar, 1);
             fence_mbar_init();
+            sgl = __ldcg(A.R.sg_logit);
         }
+        if (lane < n_act)
+            s_eoff[lane] = exp_off(lane);
         load_routing(A.R, A.E, k, lane, s_idx, s_w, cand_v, cand_e, false);
         if (lane == 0)
-            s_w[kMaxAct] = sigmoid_f(__ldcg(A.R.sg_logit));
+            s_w[kMaxAct] = sigmoid_f(sgl);
         const char *b = nullptr;
         uint32_t bytes = 0;
         if (lane < n_act) {
@@ -605,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1) down_fast_kernel(DownArgs A)
             const int inter = (lane == k) ? A.Is : A.I;
             const size_t *offs = (lane == k) ? A.src.off_sh : A.src.off;
             const uint32_t nq = (uint32_t)nr * (inter / 2), ns = (uint32_t)nr * (inter / G) * sizeof(TS);
-            unsigned char *d = smem + exp_off(lane);
+            unsigned char *d = smem + s_eoff[lane];
             bulk_g2s(d, b + offs[M_QD] + (size_t)h0 * (inter / 2), nq, &bar);
             bulk_g2s(d + nq, b + offs[M_SD] + (size_t)h0 * (inter / G) * sizeof(TS), ns, &bar);
             bulk_g2s(d + nq + ns, b + offs[M_BD] + (size_t)h0 * (inter / G) * sizeof(TS), ns, &bar);
@@ -614,7 +628,6 @@ __global__ void __launch_bounds__(kThreads, 1) down_fast_kernel(DownArgs A)
     const int pI = A.Imax + (A.Imax >> 5) * 4;
     float *as = reinterpret_cast<float *>(smem + ((wbytes + 15) & ~15u)); // [n_act][pI]
     float *asum = as + n_act * pI;                                          // [n_act][Imax/32]
-    float *dots = asum + n_act * (A.Imax >> 5);                             // [nr][n_act]
 
     pdl_wait();
     pdl_trigger();
@@ -654,27 +667,26 @@ __global__ void __launch_bounds__(kThreads, 1) down_fast_kernel(DownArgs A)
     __syncthreads();
     const bool ready = mbar_wait0(&bar);
 
-    // Half-warp items (row, expert); each lane of the half takes chunks
-    // l16, l16 + 16, ...
+    // A half-warp per output row: lane l16 takes chunks l16, l16 + 16, ... of
+    // every active expert's row and accumulates w_i * (its chunk terms) in
+    // expert order (routed by rank, then shared); one reduction per row.
     const int half = lane >> 4, l16 = lane & 15;
-    const int hw = warp * 2 + half;
-    const int n_items = nr * n_act;
-    for (int base = 0; base < n_items; base += 2 * kWarps) {
-        const int it = base + hw;
-        float dot = 0.f;
-        int hr = 0, i = 0;
-        const bool valid = ready && it < n_items;
-        if (valid) {
-            hr = it / n_act;
-            i = it - hr * n_act;
-            if (s_base[i]) {
+    for (int hr0 = 0; hr0 < nr; hr0 += 2 * kWarps) {
+        const int hr = hr0 + warp * 2 + half;
+        float acc = 0.f;
+        if (ready && hr < nr) {
+            for (int i = 0; i < n_act; ++i) {
+                if (!s_base[i])
+                    continue;
                 const int inter = (i == k) ? A.Is : A.I;
                 const int nch = inter >> 5;
                 const uint32_t nq = (uint32_t)nr * (inter / 2), ns = (uint32_t)nr * (inter / G) * sizeof(TS);
-                const unsigned char *d = smem + exp_off(i);
+                const unsigned char *d = smem + s_eoff[i];
                 const uint4 *q = reinterpret_cast<const uint4 *>(d + (size_t)hr * (inter / 2));
                 const TS *sd = reinterpret_cast<const TS *>(d + nq) + (size_t)hr * (inter / G);
                 const TS *bd = reinterpret_cast<const TS *>(d + nq + ns) + (size_t)hr * (inter / G);
+                const float wi = (i < k) ? s_w[i] : s_w[kMaxAct];
+                float part = 0.f;
                 for (int ch = l16; ch < nch; ch += 16) {
                     const float *v = as + i * pI + ch * 36;
                     float vr[32];
@@ -687,27 +699,18 @@ __global__ void __launch_bounds__(kThreads, 1) down_fast_kernel(DownArgs A)
                         vr[4 * t + 3] = f.w;
                     }
                     const int grp = (ch * 32) / G;
-                    dot += chunk_term(chunk_dot(q[ch], vr), asum[i * nchm + ch], ld_scale(sd + grp),
-                                      ld_scale(bd + grp));
+                    part += chunk_term(chunk_dot(q[ch], vr), asum[i * nchm + ch], ld_scale(sd + grp),
+                                       ld_scale(bd + grp));
                 }
+                acc = fmaf(wi, part, acc);
             }
         }
-        dot = half_warp_sum(dot);
-        if (valid && l16 == 0)
-            dots[hr * n_act + i] = dot;
-    }
-    __syncthreads();
-    if (!ready)
-        return;
-    for (int hr = threadIdx.x; hr < nr; hr += kThreads) {
-        float acc = 0.f;
-        for (int i = 0; i < n_act; ++i) {
-            const float wi = (i < k) ? s_w[i] : s_w[kMaxAct];
-            acc = fmaf(wi, dots[hr * n_act + i], acc);
+        acc = half_warp_sum(acc);
+        if (ready && hr < nr && l16 == 0) {
+            A.y[h0 + hr] = __float2bfloat16_rn(acc);
+            if (A.y32)
+                A.y32[h0 + hr] = acc;
         }
-        A.y[h0 + hr] = __float2bfloat16_rn(acc);
-        if (A.y32)
-            A.y32[h0 + hr] = acc;
     }
 }
 
