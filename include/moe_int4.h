@@ -287,9 +287,9 @@ const char *moe_last_error_message(void);
 /* Library version string. */
 const char *moe_version(void);
 
-/* Kernel selection for single-token calls, process-wide: 0 (default) uses the
- * single-token kernels (bulk-copy staged, PDL-chained) where the shape allows,
- * 1 forces the generic kernels everywhere.  The two compute the same function
+/* Kernel selection, process-wide: 0 (default) uses the single-token kernels
+ * (bulk-copy staged, PDL-chained) for T = 1 and the tcgen05 grouped GEMMs for
+ * T >= 64 where the shape allows; 1 forces the generic kernels everywhere.  The two compute the same function
  * (the pages' practice of checking fast against scalar kernels); tests compare
  * both against the CPU oracle.  MOE_ERR_INVALID_ARG for other values. */
 moe_status moe_set_kernel_path(int32_t path);

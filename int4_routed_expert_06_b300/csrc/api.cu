@@ -78,7 +78,7 @@ moe_status check_config(const moe_config *c, Shape *s)
 
 // Workspace carving, 256-byte aligned pieces.
 struct Ws {
-    size_t logits, sg, idx, w, a, hist, total;
+    size_t logits, sg, idx, w, a, hist, pre, total;
 };
 
 static int imax_of(const Shape &s) { return s.I > s.Is ? s.I : s.Is; }
@@ -93,6 +93,9 @@ static Ws layer_ws(const Shape &s, int T)
     w.w = o;      o += align256(sizeof(float) * (size_t)T * s.k);
     w.a = o;      o += align256(sizeof(float) * (size_t)T * (s.k + 1) * imax_of(s));
     w.hist = o;   o += align256(sizeof(int32_t) * (size_t)bucket_chunks(T * s.k) * s.E);
+    w.pre = o;
+    if (T >= prefill::kMinTokens && s.H % 128 == 0 && s.I % 64 == 0 && s.Is % 64 == 0 && s.Is > 0)
+        o += align256(prefill::layout(s, T).total);
     w.total = o;
     return w;
 }
@@ -372,6 +375,10 @@ moe_status moe_experts_forward(const moe_config *cfg, const moe_layer *L, const 
         return fail(MOE_ERR_OOM, "moe_experts_forward: workspace needs %zu bytes (256-byte aligned), got %zu",
                     w.total, ws_bytes);
     float *a = reinterpret_cast<float *>(static_cast<char *>(workspace) + w.a);
+    if (prefill::eligible(s, T) && w.total > w.pre)
+        return cuda_check(prefill::experts_forward(s, src, x, T, topk_idx, topk_w, shared_gate_logit, y, y_f32,
+                                                   static_cast<char *>(workspace) + w.pre, stream),
+                          "moe_experts_forward: grouped GEMM");
     if (T == 1 && fast::eligible(s)) {
         fast::Routing R{nullptr, topk_idx, topk_w, nullptr, nullptr, shared_gate_logit};
         return cuda_check(fast::launch_experts_fast(s, x, src, R, a, y, y_f32, stream), "moe_experts_forward");

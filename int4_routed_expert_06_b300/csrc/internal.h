@@ -65,4 +65,20 @@ cudaError_t launch_experts_fast(const Shape &s, const void *x, const ExpertSrc &
                                 void *y, float *y32, cudaStream_t st);
 } // namespace fast
 
+namespace prefill {
+// Calls with at least this many tokens take the grouped-GEMM path.
+constexpr int kMinTokens = 64;
+// Byte offsets of the prefill buffers inside a workspace region.
+struct Layout {
+    size_t counts, offsets, perm_tok, perm_rank, hist, inv, wpair, units_gu, units_dn, n_units, xs, act, pout,
+        total;
+};
+Layout layout(const Shape &s, int T);
+// bf16 activations, H a multiple of 128, I and I_s multiples of 64, a shared
+// expert, a Blackwell (sm_10x) device, T >= kMinTokens.
+bool eligible(const Shape &s, int T);
+cudaError_t experts_forward(const Shape &s, const ExpertSrc &src, const void *x, int T, const int32_t *idx,
+                            const float *topk_w, const float *sg, void *y, float *y32, char *ws, cudaStream_t st);
+} // namespace prefill
+
 } // namespace moe

@@ -3,6 +3,7 @@
 #include "api.cu"
 #include "kernels_decode.cu"
 #include "kernels_fast.cu"
+#include "prefill.cu"
 #include "bucket.cu"
 #include "slot_pool.cu"
 #include "noalloc.cu"

@@ -1,0 +1,701 @@
+// Many-token (prefill) path of the routed int4 MoE layer: the expert MLPs
+// as grouped GEMMs on the 5th-generation tensor cores (tcgen05, TMEM
+// accumulators, TMA-fed operands).
+//
+//   route      router logits and top-k per token (the generic router kernels)
+//   bucket     stable counting sort of the T*k (token, rank) pairs by expert
+//   gather     X_sorted[p] = x[token of pair p]           (bf16 rows)
+//   pairs      per sorted row: its routing weight, and the inverse permutation
+//   plan       work units (expert, feature tile, token chunk), largest first
+//   gemm gu    act[p, f] = silu(W_g x_p)_f * (W_u x_p)_f   (bf16)
+//   gemm down  P[p, h]   = w_p * (W_d act_p)_h             (fp32)
+//   combine    y[t] = sum_r P[pair(t, r)] + P[shared row t], fixed order
+//
+// The GEMMs run "swap-AB": the M = 128 side of each MMA is a tile of weight
+// rows, dequantised from int4 by four warps straight into the 128-byte
+// swizzled K-major shared-memory layout the MMA reads; the N side is the
+// expert's tokens (rounded up to 16, at most 256 per unit), brought in by TMA
+// with the matching swizzle.  Skewed routing then costs at most 15 padded
+// token columns per unit instead of a 128-row tile.  The shared expert is one
+// more group, over all T tokens.
+#include <cuda.h>
+#include <mutex>
+
+#include "internal.h"
+
+namespace moe {
+namespace prefill {
+
+constexpr int kNch = 256;        // tokens per unit (MMA N <= 256)
+constexpr int kBK = 64;          // K per pipeline stage (one 128-byte swizzle atom of bf16)
+constexpr int kStages = 4;
+constexpr int kBoxRows = 32;     // TMA box: 32 rows x 64 bf16
+constexpr int kThreads = 320;    // warps 0-3 dequant, 4 TMA, 5 MMA, 6-9 epilogue
+constexpr uint32_t kATile = 128 * 128;         // 16 KB
+constexpr uint32_t kBTile = kNch * 128;        // 32 KB
+constexpr uint32_t kSmem = kStages * (kATile + kBTile) + 1024;
+constexpr uint64_t kWaitNs = 500ull * 1000 * 1000; // 0.5 s bound on any single wait
+
+struct Unit {
+    int e;    // expert id, -1 = shared expert
+    int ft;   // feature tile: gate/up 64 features (128 interleaved rows), down 128 output rows
+    int j0;   // first row of the unit in the B source (sorted pair index, or token for the shared expert)
+    int n;    // tokens (1..256)
+};
+
+// ------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t gtime()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void bar_init(uint64_t *b, uint32_t n)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ void bar_arrive(uint64_t *b)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+
+__device__ __forceinline__ void bar_expect(uint64_t *b, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool bar_try(uint64_t *b, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_u32(b)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// Wait until the phase of parity `parity` has completed, for at most kWaitNs.
+__device__ __forceinline__ bool bar_wait(uint64_t *b, uint32_t parity)
+{
+    if (bar_try(b, parity))
+        return true;
+    const uint64_t t0 = gtime();
+    for (;;) {
+        for (int i = 0; i < 32; ++i)
+            if (bar_try(b, parity))
+                return true;
+        if (gtime() - t0 > kWaitNs) {
+            record_error(MOE_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// tcgen05 shared-memory matrix descriptor: K-major, 128-byte swizzle,
+// 8-row groups 1024 bytes apart (SBO), version 1.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFF) >> 4);          // start address
+    d |= (uint64_t)1 << 16;                           // leading byte offset (unused with this swizzle)
+    d |= (uint64_t)(1024 >> 4) << 32;                 // stride byte offset
+    d |= (uint64_t)1 << 46;                           // descriptor version
+    d |= (uint64_t)2 << 61;                           // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 x bf16 -> fp32, both K-major.
+__host__ __device__ __forceinline__ uint32_t idesc_bf16(int M, int N)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+                   "=r"(r[15])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// ------------------------------------------------------------ small kernels
+
+// X_sorted[p] = x[perm_tok[p]], rows of H bf16 (16-byte copies).
+__global__ void gather_rows_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ perm_tok, int P,
+                                   int row16, uint4 *__restrict__ xs)
+{
+    const long n = (long)P * row16;
+    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+        const long p = i / row16, c = i - p * row16;
+        xs[i] = __ldg(x + (long)perm_tok[p] * row16 + c);
+    }
+}
+
+// Per sorted row: the routing weight (shared rows: sigmoid of the gate logit)
+// and the inverse permutation inv[t*k + r] = sorted index of pair (t, r).
+__global__ void pair_prep_kernel(const int32_t *__restrict__ perm_tok, const int32_t *__restrict__ perm_rank,
+                                 const float *__restrict__ topk_w, const float *__restrict__ sg, int T, int k,
+                                 float *__restrict__ wpair, int32_t *__restrict__ inv)
+{
+    const int P = T * k;
+    for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < P + T; p += gridDim.x * blockDim.x) {
+        if (p < P) {
+            const int t = perm_tok[p], r = perm_rank[p];
+            wpair[p] = topk_w[t * k + r];
+            inv[t * k + r] = p;
+        } else {
+            wpair[p] = sg ? 1.f / (1.f + __expf(-sg[p - P])) : 1.f;
+        }
+    }
+}
+
+// One CTA: rank the experts by token count (descending, ties by id), lay out
+// their units in that order after the shared expert's.  Unit order within an
+// expert: token chunk major, feature tile minor.  E <= 1024.
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ counts,
+                                                    const int32_t *__restrict__ offsets, int E, int T,
+                                                    int n_ft, int n_ft_sh, int has_shared, Unit *__restrict__ units,
+                                                    int32_t *__restrict__ n_units)
+{
+    __shared__ int s_cnt[1024];
+    __shared__ int s_ord[1024];
+    __shared__ int s_scan[1024];
+    const int e = threadIdx.x;
+    s_cnt[e] = e < E ? counts[e] : -1;
+    __syncthreads();
+    int rank = 0;
+    if (e < E) {
+        const int c = s_cnt[e];
+        for (int j = 0; j < E; ++j) {
+            const int cj = s_cnt[j];
+            rank += (cj > c || (cj == c && j < e)) ? 1 : 0;
+        }
+        s_ord[rank] = e;
+    }
+    __syncthreads();
+    // units of the expert at rank position e
+    int nu = 0, ex = -1;
+    if (e < E) {
+        ex = s_ord[e];
+        nu = n_ft * ((s_cnt[ex] + kNch - 1) / kNch);
+    }
+    s_scan[e] = nu;
+    __syncthreads();
+    for (int o = 1; o < 1024; o <<= 1) { // inclusive scan (Hillis-Steele)
+        const int v = e >= o ? s_scan[e - o] : 0;
+        __syncthreads();
+        s_scan[e] += v;
+        __syncthreads();
+    }
+    const int sh_units = has_shared ? n_ft_sh * ((T + kNch - 1) / kNch) : 0;
+    if (e == 0 && has_shared) {
+        int u = 0;
+        for (int c0 = 0; c0 < T; c0 += kNch)
+            for (int ft = 0; ft < n_ft_sh; ++ft)
+                units[u++] = {-1, ft, c0, min(kNch, T - c0)};
+    }
+    if (e < E && nu > 0) {
+        int u = sh_units + s_scan[e] - nu;
+        const int base = offsets[ex], cnt = s_cnt[ex];
+        for (int c0 = 0; c0 < cnt; c0 += kNch)
+            for (int ft = 0; ft < n_ft; ++ft)
+                units[u++] = {ex, ft, base + c0, min(kNch, cnt - c0)};
+    }
+    if (e == 1023)
+        *n_units = sh_units + s_scan[1023];
+}
+
+// y[t, h] = sum_r P[inv[t, r], h] + P[T*k + t, h]; bf16 y and optional fp32.
+__global__ void combine_kernel(const float *__restrict__ P, const int32_t *__restrict__ inv, int T, int k, int H,
+                               int has_shared, __nv_bfloat16 *__restrict__ y, float *__restrict__ y32)
+{
+    const long n = (long)T * H;
+    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+        const int t = (int)(i / H), h = (int)(i - (long)t * H);
+        float acc = 0.f;
+        for (int r = 0; r < k; ++r)
+            acc += __ldg(P + (long)inv[t * k + r] * H + h);
+        if (has_shared)
+            acc += __ldg(P + ((long)T * k + t) * H + h);
+        y[i] = __float2bfloat16_rn(acc);
+        if (y32)
+            y32[i] = acc;
+    }
+}
+
+// ------------------------------------------------------------ grouped GEMM
+
+struct GemmArgs {
+    const Unit *units;
+    const int32_t *n_units;
+    ExpertSrc src;
+    int mode;            // 0 gate/up, 1 down
+    int H, I, Is, G, T, k;
+    int act_ld;          // row length of the activation buffer (max(I, Is))
+    const float *wpair;  // down: weight of each sorted row
+    __nv_bfloat16 *act;  // gate/up output [T*k + T, act_ld]
+    float *pout;         // down output [T*k + T, H]
+};
+
+// 128 weight rows x 64 K of one stage, dequantised to bf16 into the swizzled
+// K-major tile (row r at r*128 bytes, 16-byte chunk c at position c ^ (r&7)).
+template <typename TS>
+__device__ __forceinline__ void dequant_row(const uint32_t *__restrict__ q, const TS *__restrict__ sc,
+                                            const TS *__restrict__ bi, int k0, int G, unsigned char *tile, int r)
+{
+    const uint4 w0 = __ldg(reinterpret_cast<const uint4 *>(q + k0 / 8));
+    const uint4 w1 = __ldg(reinterpret_cast<const uint4 *>(q + k0 / 8) + 1);
+    const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    unsigned char *row = tile + r * 128;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int g = (k0 + 32 * half) / G;
+        const float s = to_f32(sc[g]), b = to_f32(bi[g]);
+        const float s16 = 16.f * s, b16 = b - s16;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) { // 16-byte chunk = 8 columns = one code word
+            const uint32_t word = w[half * 4 + cc];
+            const uint32_t lo = ((word << 3) & 0x78787878u) | 0x80808080u;
+            const uint32_t hi = ((word >> 1) & 0x78787878u) | 0x80808080u;
+            uint32_t packed[4];
+#pragma unroll
+            for (int bb = 0; bb < 4; ++bb) {
+                const uint32_t sel = 0x7044u | (uint32_t)(bb << 8);
+                const float f0 = __uint_as_float(__byte_perm(lo, 0x3F000000u, sel)); // 1 + q/16, column 2bb
+                const float f1 = __uint_as_float(__byte_perm(hi, 0x3F000000u, sel)); // column 2bb + 1
+                const float2 wv = __ffma2_rn(make_float2(f0, f1), make_float2(s16, s16), make_float2(b16, b16));
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(wv.x, wv.y);
+                packed[bb] = *reinterpret_cast<uint32_t *>(&h2);
+            }
+            const int c = half * 4 + cc;
+            *reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4)) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        }
+    }
+}
+
+template <typename TS>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_constant__ CUtensorMap tm_shared,
+                        GemmArgs A)
+{
+    extern __shared__ unsigned char smem_raw[];
+    __shared__ uint64_t a_full[kStages], b_full[kStages], empty[kStages], acc_full[2], acc_empty[2];
+    __shared__ uint32_t tmem_base;
+    __shared__ volatile int s_abort;
+
+    unsigned char *smem = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    unsigned char *a_tiles = smem;
+    unsigned char *b_tiles = smem + kStages * kATile;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nu = *A.n_units;
+    const int G = A.G;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            bar_init(&a_full[s], 128);
+            bar_init(&b_full[s], 1);
+            bar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            bar_init(&acc_full[b], 1);
+            bar_init(&acc_empty[b], 128);
+        }
+        s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 5) { // TMEM: 2 accumulators x 256 fp32 columns
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&tmem_base))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+
+    auto kdim = [&](const Unit &u) { return A.mode == 0 ? A.H : (u.e < 0 ? A.Is : A.I); };
+
+    if (warp < 4) {
+        // ---------------- dequant producers: thread r owns tile row r
+        const int r = threadIdx.x;
+        int stage = 0;
+        uint32_t ph = 0;
+        for (int ui = blockIdx.x; ui < nu && !s_abort; ui += gridDim.x) {
+            const Unit u = A.units[ui];
+            const char *base;
+            const size_t *off;
+            if (u.e < 0) {
+                base = A.src.shared;
+                off = A.src.off_sh;
+            } else {
+                const int slot = A.src.table[u.e];
+                base = (slot >= 0 && slot < A.src.n_slots) ? A.src.pool + (size_t)slot * A.src.stride : nullptr;
+                off = A.src.off;
+                if (!base && r == 0)
+                    record_error(MOE_ERR_NOT_RESIDENT);
+            }
+            const int K = kdim(u);
+            const uint32_t *q;
+            const TS *sc, *bi;
+            if (A.mode == 0) { // interleaved: even rows gate, odd rows up, feature ft*64 + r/2
+                const int f = u.ft * 64 + (r >> 1);
+                const int m_q = (r & 1) ? M_QU : M_QG, m_s = (r & 1) ? M_SU : M_SG, m_b = (r & 1) ? M_BU : M_BG;
+                q = base ? reinterpret_cast<const uint32_t *>(base + off[m_q]) + (size_t)f * (K / 8) : nullptr;
+                sc = base ? reinterpret_cast<const TS *>(base + off[m_s]) + (size_t)f * (K / G) : nullptr;
+                bi = base ? reinterpret_cast<const TS *>(base + off[m_b]) + (size_t)f * (K / G) : nullptr;
+            } else {
+                const int h = u.ft * 128 + r;
+                q = base ? reinterpret_cast<const uint32_t *>(base + off[M_QD]) + (size_t)h * (K / 8) : nullptr;
+                sc = base ? reinterpret_cast<const TS *>(base + off[M_SD]) + (size_t)h * (K / G) : nullptr;
+                bi = base ? reinterpret_cast<const TS *>(base + off[M_BD]) + (size_t)h * (K / G) : nullptr;
+            }
+            for (int k0 = 0; k0 < K; k0 += kBK) {
+                if (!bar_wait(&empty[stage], ph ^ 1)) {
+                    s_abort = 1;
+                    break;
+                }
+                unsigned char *tile = a_tiles + stage * kATile;
+                if (q) {
+                    dequant_row<TS>(q, sc, bi, k0, G, tile, r);
+                } else {
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4 *>(tile + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                bar_arrive(&a_full[stage]);
+                if (++stage == kStages) {
+                    stage = 0;
+                    ph ^= 1;
+                }
+            }
+            if (s_abort)
+                break;
+        }
+    } else if (warp == 4) {
+        // ---------------- TMA producer for the token operand
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t ph = 0;
+            for (int ui = blockIdx.x; ui < nu && !s_abort; ui += gridDim.x) {
+                const Unit u = A.units[ui];
+                const int K = kdim(u);
+                const int nbox = (u.n + kBoxRows - 1) / kBoxRows;
+                // rows: gate/up routed -> sorted x; gate/up shared -> x; down -> activations
+                const CUtensorMap *map = (A.mode == 0 && u.e < 0) ? &tm_shared : &tm_rows;
+                const int row0 = (A.mode == 1 && u.e < 0) ? A.T * A.k + u.j0 : u.j0;
+                for (int k0 = 0; k0 < K; k0 += kBK) {
+                    if (!bar_wait(&empty[stage], ph ^ 1)) {
+                        s_abort = 1;
+                        break;
+                    }
+                    bar_expect(&b_full[stage], (uint32_t)nbox * kBoxRows * 128);
+                    unsigned char *tile = b_tiles + stage * kBTile;
+                    for (int bx = 0; bx < nbox; ++bx)
+                        tma_load_2d(tile + bx * kBoxRows * 128, map, k0, row0 + bx * kBoxRows, &b_full[stage]);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
+        }
+    } else if (warp == 5) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            int stage = 0, acc = 0;
+            uint32_t ph = 0, acc_ph = 0;
+            for (int ui = blockIdx.x; ui < nu && !s_abort; ui += gridDim.x) {
+                const Unit u = A.units[ui];
+                const int K = kdim(u);
+                const int N = (u.n + 15) & ~15;
+                const uint32_t idesc = idesc_bf16(128, N);
+                const uint32_t d_tmem = tmem + (uint32_t)(acc * 256);
+                if (!bar_wait(&acc_empty[acc], acc_ph ^ 1)) {
+                    s_abort = 1;
+                    break;
+                }
+                tc_fence_after();
+                for (int k0 = 0; k0 < K; k0 += kBK) {
+                    if (!bar_wait(&a_full[stage], ph) || !bar_wait(&b_full[stage], ph)) {
+                        s_abort = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(a_tiles + stage * kATile);
+                    const uint32_t b_addr = smem_u32(b_tiles + stage * kBTile);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        mma_bf16(d_tmem, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32), idesc,
+                                 (k0 > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&empty[stage]);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        ph ^= 1;
+                    }
+                }
+                if (s_abort)
+                    break;
+                mma_commit(&acc_full[acc]);
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_ph ^= 1;
+                }
+            }
+        }
+    } else {
+        // ---------------- epilogue: warps 6..9, TMEM lanes 32*(warp%4) ..
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane; // tile row of this thread
+        int acc = 0;
+        uint32_t acc_ph = 0;
+        for (int ui = blockIdx.x; ui < nu && !s_abort; ui += gridDim.x) {
+            const Unit u = A.units[ui];
+            if (!bar_wait(&acc_full[acc], acc_ph)) {
+                s_abort = 1;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t t_row = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * 256);
+            const int rowb = (u.e < 0) ? A.T * A.k + u.j0 : u.j0; // first output row of the unit
+            for (int c0 = 0; c0 < u.n; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld16(t_row + (uint32_t)c0, v);
+                if (A.mode == 0) {
+                    const int f = u.ft * 64 + (r >> 1);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float mine = __uint_as_float(v[j]);
+                        const float other = __shfl_xor_sync(0xFFFFFFFFu, mine, 1);
+                        if (!(r & 1) && c0 + j < u.n) {
+                            const float g = mine, up = other;
+                            const float a = g / (1.f + __expf(-g)) * up;
+                            A.act[(size_t)(rowb + c0 + j) * A.act_ld + f] = __float2bfloat16_rn(a);
+                        }
+                    }
+                } else {
+                    const int h = u.ft * 128 + r;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (c0 + j < u.n) {
+                            const int row = rowb + c0 + j;
+                            A.pout[(size_t)row * A.H + h] = A.wpair[row] * __uint_as_float(v[j]);
+                        }
+                }
+            }
+            tc_fence_before();
+            bar_arrive(&acc_empty[acc]);
+            if (++acc == 2) {
+                acc = 0;
+                acc_ph ^= 1;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+    }
+}
+
+// ------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2D map over a row-major bf16 matrix [rows, cols]: boxes of 32 rows x 64
+// columns with the 128-byte swizzle.
+static bool make_map(CUtensorMap *m, const void *base, long rows, int cols)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBoxRows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static int sm_count()
+{
+    int dev = 0, v = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    return v > 0 ? v : 148;
+}
+
+static size_t a256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+Layout layout(const Shape &s, int T)
+{
+    Layout L{};
+    const long P = (long)T * s.k;
+    const int imax = s.I > s.Is ? s.I : s.Is;
+    const int nft = s.I / 64, nft_sh = s.Is / 64, hft = s.H / 128;
+    const long max_u_gu = (long)nft * (s.E + P / kNch + 1) + (long)nft_sh * (T / kNch + 1);
+    const long max_u_dn = (long)hft * (s.E + P / kNch + 1) + (long)hft * (T / kNch + 1);
+    size_t o = 0;
+    L.counts = o;   o += a256(4 * (size_t)s.E);
+    L.offsets = o;  o += a256(4 * (size_t)(s.E + 1));
+    L.perm_tok = o; o += a256(4 * (size_t)P);
+    L.perm_rank = o; o += a256(4 * (size_t)P);
+    L.hist = o;     o += a256(4 * (size_t)bucket_chunks((int)P) * s.E);
+    L.inv = o;      o += a256(4 * (size_t)P);
+    L.wpair = o;    o += a256(4 * (size_t)(P + T));
+    L.units_gu = o; o += a256(sizeof(Unit) * (size_t)max_u_gu);
+    L.units_dn = o; o += a256(sizeof(Unit) * (size_t)max_u_dn);
+    L.n_units = o;  o += 256;
+    L.xs = o;       o += a256(2 * (size_t)P * s.H + 2 * (size_t)kNch * s.H);   // + slack rows for full boxes
+    L.act = o;      o += a256(2 * (size_t)(P + T + kNch) * imax);
+    L.pout = o;     o += a256(4 * (size_t)(P + T) * s.H);
+    L.total = o;
+    return L;
+}
+
+bool eligible(const Shape &s, int T)
+{
+    if (kernel_path() != 0 || T < kMinTokens || T > 65536)
+        return false;
+    if (s.act != MOE_BF16 || s.H % 128 || s.I % 64 || s.Is % 64 || s.Is == 0)
+        return false;
+    if (encode_fn() == nullptr)
+        return false;
+    int dev = 0, major = 0, minor = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    return major == 10;
+}
+
+template <typename TS>
+static cudaError_t gemm_go(const CUtensorMap &rows, const CUtensorMap &shared, const GemmArgs &g, cudaStream_t st)
+{
+    static int cur = 0;
+    cudaError_t e = ensure_smem(grouped_gemm_kernel<TS>, kSmem, &cur);
+    if (e != cudaSuccess)
+        return e;
+    grouped_gemm_kernel<TS><<<sm_count(), kThreads, kSmem, st>>>(rows, shared, g);
+    return cudaGetLastError();
+}
+
+// Expert part of the layer for T tokens given the routing (idx, w, sg).
+cudaError_t experts_forward(const Shape &s, const ExpertSrc &src, const void *x, int T, const int32_t *idx,
+                            const float *topk_w, const float *sg, void *y, float *y32, char *ws, cudaStream_t st)
+{
+    const Layout L = layout(s, T);
+    const long P = (long)T * s.k;
+    const int imax = s.I > s.Is ? s.I : s.Is;
+    int32_t *counts = reinterpret_cast<int32_t *>(ws + L.counts);
+    int32_t *offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
+    int32_t *perm_tok = reinterpret_cast<int32_t *>(ws + L.perm_tok);
+    int32_t *perm_rank = reinterpret_cast<int32_t *>(ws + L.perm_rank);
+    int32_t *inv = reinterpret_cast<int32_t *>(ws + L.inv);
+    float *wpair = reinterpret_cast<float *>(ws + L.wpair);
+    Unit *u_gu = reinterpret_cast<Unit *>(ws + L.units_gu);
+    Unit *u_dn = reinterpret_cast<Unit *>(ws + L.units_dn);
+    int32_t *n_units = reinterpret_cast<int32_t *>(ws + L.n_units);
+    __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(ws + L.xs);
+    __nv_bfloat16 *act = reinterpret_cast<__nv_bfloat16 *>(ws + L.act);
+    float *pout = reinterpret_cast<float *>(ws + L.pout);
+
+    cudaError_t e = launch_bucket(s, idx, T, counts, offsets, perm_tok, perm_rank,
+                                  reinterpret_cast<int32_t *>(ws + L.hist), st);
+    if (e != cudaSuccess)
+        return e;
+    const int row16 = s.H / 8;
+    gather_rows_kernel<<<4 * sm_count(), 256, 0, st>>>(static_cast<const uint4 *>(x), perm_tok, (int)P, row16,
+                                                      reinterpret_cast<uint4 *>(xs));
+    pair_prep_kernel<<<(int)((P + T + 255) / 256), 256, 0, st>>>(perm_tok, perm_rank, topk_w, sg, T, s.k, wpair,
+                                                                 inv);
+    plan_kernel<<<1, 1024, 0, st>>>(counts, offsets, s.E, T, s.I / 64, s.Is / 64, 1, u_gu, n_units);
+    plan_kernel<<<1, 1024, 0, st>>>(counts, offsets, s.E, T, s.H / 128, s.H / 128, 1, u_dn, n_units + 1);
+    if ((e = cudaGetLastError()) != cudaSuccess)
+        return e;
+
+    CUtensorMap m_xs, m_x, m_act;
+    if (!make_map(&m_xs, xs, P + kNch, s.H) || !make_map(&m_x, x, T, s.H) ||
+        !make_map(&m_act, act, P + T + kNch, imax))
+        return cudaErrorInvalidValue;
+    GemmArgs g{};
+    g.src = src;
+    g.H = s.H;
+    g.I = s.I;
+    g.Is = s.Is;
+    g.G = s.G;
+    g.T = T;
+    g.k = s.k;
+    g.act_ld = imax;
+    g.wpair = wpair;
+    g.act = act;
+    g.pout = pout;
+    g.units = u_gu;
+    g.n_units = n_units;
+    g.mode = 0;
+    e = (s.qscale == MOE_F16) ? gemm_go<__half>(m_xs, m_x, g, st) : gemm_go<float>(m_xs, m_x, g, st);
+    if (e != cudaSuccess)
+        return e;
+    g.units = u_dn;
+    g.n_units = n_units + 1;
+    g.mode = 1;
+    e = (s.qscale == MOE_F16) ? gemm_go<__half>(m_act, m_act, g, st) : gemm_go<float>(m_act, m_act, g, st);
+    if (e != cudaSuccess)
+        return e;
+    combine_kernel<<<4 * sm_count(), 256, 0, st>>>(pout, inv, T, s.k, s.H, 1, static_cast<__nv_bfloat16 *>(y), y32);
+    return cudaGetLastError();
+}
+
+} // namespace prefill
+} // namespace moe
