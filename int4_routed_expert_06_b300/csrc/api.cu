@@ -27,6 +27,7 @@ moe_status cuda_check(cudaError_t e, const char *what)
 {
     if (e == cudaSuccess)
         return MOE_OK;
+    cudaGetLastError(); // a rejected launch also sets the last-error state; leave it clear for the caller
     return fail(e == cudaErrorMemoryAllocation ? MOE_ERR_OOM : MOE_ERR_CUDA, "%s: %s", what,
                 cudaGetErrorString(e));
 }
@@ -78,7 +79,7 @@ moe_status check_config(const moe_config *c, Shape *s)
 
 // Workspace carving, 256-byte aligned pieces.
 struct Ws {
-    size_t logits, sg, idx, w, a, hist, pre, total;
+    size_t logits, sg, idx, w, a, tok, hist, pre, total;
 };
 
 static int imax_of(const Shape &s) { return s.I > s.Is ? s.I : s.Is; }
@@ -92,6 +93,7 @@ static Ws layer_ws(const Shape &s, int T)
     w.idx = o;    o += align256(sizeof(int32_t) * (size_t)T * s.k);
     w.w = o;      o += align256(sizeof(float) * (size_t)T * s.k);
     w.a = o;      o += align256(sizeof(float) * (size_t)T * (s.k + 1) * imax_of(s));
+    w.tok = o;    o += T == 1 ? align256(tok::bufs_bytes(s)) : 0;
     w.hist = o;   o += align256(sizeof(int32_t) * (size_t)bucket_chunks(T * s.k) * s.E);
     w.pre = o;
     if (T >= prefill::kMinTokens && s.H % 128 == 0 && s.I % 64 == 0 && s.Is % 64 == 0 && s.Is > 0)
@@ -238,8 +240,9 @@ moe_status moe_route(const moe_config *cfg, const void *x, int32_t T, const void
         logits = reinterpret_cast<float *>(static_cast<char *>(workspace) + w.logits);
     }
     cudaError_t e;
-    if (T == 1 && fast::eligible(s))
-        e = fast::launch_router_fast(s, x, w_router, router_bias, w_shared_gate, logits, shared_gate_logit, stream);
+    if (T == 1 && tok::eligible(s))
+        e = tok::launch_router(s, x, w_router, router_bias, w_shared_gate, logits, 0, 1, shared_gate_logit,
+                               nullptr, 0, stream);
     else
         e = launch_router(s, x, T, w_router, router_bias, s.Is > 0 ? w_shared_gate : nullptr, logits,
                           shared_gate_logit, stream);
@@ -379,9 +382,14 @@ moe_status moe_experts_forward(const moe_config *cfg, const moe_layer *L, const 
         return cuda_check(prefill::experts_forward(s, src, x, T, topk_idx, topk_w, shared_gate_logit, y, y_f32,
                                                    static_cast<char *>(workspace) + w.pre, stream),
                           "moe_experts_forward: grouped GEMM");
-    if (T == 1 && fast::eligible(s)) {
-        fast::Routing R{nullptr, topk_idx, topk_w, nullptr, nullptr, shared_gate_logit};
-        return cuda_check(fast::launch_experts_fast(s, x, src, R, a, y, y_f32, stream), "moe_experts_forward");
+    if (T == 1 && tok::eligible(s)) {
+        const tok::Bufs b = tok::bufs_carve(s, static_cast<char *>(workspace) + w.tok);
+        cudaError_t e = tok::launch_router(s, x, nullptr, nullptr, nullptr, nullptr, 0, 0, nullptr, b.xrec, b.xrs,
+                                           stream);
+        if (e != cudaSuccess)
+            return cuda_check(e, "moe_experts_forward: x records");
+        tok::Routing R{nullptr, 0, topk_idx, topk_w, nullptr, nullptr, shared_gate_logit};
+        return cuda_check(tok::launch_experts(s, b, src, R, y, y_f32, stream), "moe_experts_forward");
     }
     const int n_act = s.k + (s.Is > 0 ? 1 : 0);
     cudaError_t e = launch_gateup(s, x, T, s.k, n_act, topk_idx, src, a, imax_of(s), stream);
@@ -414,7 +422,7 @@ moe_status moe_layer_forward(const moe_config *cfg, const moe_layer *L, const vo
     int32_t *idx = topk_idx_out ? topk_idx_out : reinterpret_cast<int32_t *>(ws + w.idx);
     float *tw = topk_w_out ? topk_w_out : reinterpret_cast<float *>(ws + w.w);
     float *sg = s.Is > 0 ? reinterpret_cast<float *>(ws + w.sg) : nullptr;
-    if (T == 1 && fast::eligible(s)) {
+    if (T == 1 && tok::eligible(s)) {
         if (!aligned(x, 16) || !L->w_router || !aligned(L->w_router, 16) || !L->w_shared_gate ||
             !aligned(L->w_shared_gate, 16) || !y)
             return fail(MOE_ERR_INVALID_ARG, "moe_layer_forward: x, y, w_router and w_shared_gate must be non-NULL "
@@ -422,14 +430,13 @@ moe_status moe_layer_forward(const moe_config *cfg, const moe_layer *L, const vo
         ExpertSrc src;
         if ((st = make_src(cfg, s, L, &src, "moe_layer_forward")) != MOE_OK)
             return st;
-        float *logits = reinterpret_cast<float *>(ws + w.logits);
-        cudaError_t e = fast::launch_router_fast(s, x, L->w_router, L->router_bias, L->w_shared_gate, logits, sg,
-                                                 stream);
+        const tok::Bufs b = tok::bufs_carve(s, ws + w.tok);
+        cudaError_t e = tok::launch_router(s, x, L->w_router, L->router_bias, L->w_shared_gate, b.lg, b.lgs,
+                                           tok::kRep, nullptr, b.xrec, b.xrs, stream);
         if (e != cudaSuccess)
             return cuda_check(e, "moe_layer_forward: router");
-        fast::Routing R{logits, nullptr, nullptr, idx, tw, sg};
-        float *a = reinterpret_cast<float *>(ws + w.a);
-        return cuda_check(fast::launch_experts_fast(s, x, src, R, a, y, y_f32, stream), "moe_layer_forward: experts");
+        tok::Routing R{b.lg, b.lgs, nullptr, nullptr, idx, tw, nullptr};
+        return cuda_check(tok::launch_experts(s, b, src, R, y, y_f32, stream), "moe_layer_forward: experts");
     }
     st = moe_route(cfg, x, T, L->w_router, L->router_bias, s.Is > 0 ? L->w_shared_gate : nullptr, idx, tw, sg,
                    reinterpret_cast<float *>(ws + w.logits), nullptr, 0, stream);

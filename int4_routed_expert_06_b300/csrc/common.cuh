@@ -78,11 +78,13 @@ __device__ __forceinline__ float sigmoid_f(float v) { return 1.0f / (1.0f + __ex
 
 // Raise a kernel's dynamic shared-memory limit to at least `bytes`, calling
 // the runtime only when the limit grows (so that repeated launches, including
-// those made during stream capture, do not touch function attributes).
+// those made during stream capture, do not touch function attributes).  The
+// limit is raised even below 48 KB: the default covers static plus dynamic
+// shared memory, so a kernel with static arrays needs it sooner.
 template <typename F>
 static cudaError_t ensure_smem(F *kern, size_t bytes, int *cur)
 {
-    if ((int)bytes <= *cur || bytes <= 48 * 1024)
+    if ((int)bytes <= *cur)
         return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (e == cudaSuccess)

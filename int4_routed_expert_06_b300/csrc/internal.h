@@ -42,28 +42,51 @@ cudaError_t launch_bucket(const Shape &s, const int32_t *idx, int T, int32_t *co
                           int32_t *chunk_hist, cudaStream_t st);
 int bucket_chunks(int pairs);
 
-// 0 = use the single-token fast kernels where eligible, 1 = generic kernels only.
+// 0 = use the single-token kernels where eligible, 1 = generic kernels only.
 int kernel_path();
 
-namespace fast {
-// Routing of one token for the fast expert kernels: either top-k from logits
-// (every CTA recomputes it) or given idx / w.
+namespace tok {
+// Small per-call buffers that every CTA of a kernel reads are written in
+// kRep copies; CTA c reads copy c % kRep, which spreads the reads of 148
+// SMs over more L2 lines.
+constexpr int kRep = 8;
+// Per-call scratch of the single-token path, carved from the workspace.
+struct Bufs {
+    float *lg;           // [kRep][lgs]: the E logits, then the shared-gate logit at [E]
+    int lgs;             // floats per logits copy
+    unsigned char *xrec; // [kRep][xrs]: fixed-point records of x
+    size_t xrs;          // bytes per x copy
+    float *a;            // [kRep][as]: SwiGLU activations [k+1][Imax]
+    size_t as;           // floats per a copy
+};
+size_t bufs_bytes(const Shape &s);
+Bufs bufs_carve(const Shape &s, char *base);
+// Routing of one token for the single-token expert kernels: either top-k
+// from logits (every CTA recomputes it) or given idx / w.
 struct Routing {
-    const float *logits;     // [E] or NULL when idx/w are given
+    const float *logits;     // copy 0 of the logits (+ shared-gate logit at [E]), or NULL when idx/w are given
+    int lgs;                 // floats between logits copies
     const int32_t *idx;      // [k] given, or NULL
     const float *w;          // [k] given, or NULL
     int32_t *idx_out;        // [k] written by CTA 0 of gate/up (logits mode), or NULL
     float *w_out;            // [k]
-    const float *sg_logit;   // [1] shared-gate logit
+    const float *sg_logit;   // [1] shared-gate logit when logits == NULL
 };
-// Shapes the single-token kernels handle (bf16 activations, H in {1024, 2048,
-// 4096}, a shared expert, 16-byte scale rows, shares that fit shared memory).
+// Shapes the single-token kernels handle (bf16 activations and router,
+// H in {1024, 2048}, a shared expert, 16-byte scale rows, per-CTA shares that
+// fit shared memory).
 bool eligible(const Shape &s);
-cudaError_t launch_router_fast(const Shape &s, const void *x, const void *w_router, const float *bias,
-                               const void *w_sg, float *logits, float *sg, cudaStream_t st);
-cudaError_t launch_experts_fast(const Shape &s, const void *x, const ExpertSrc &src, const Routing &R, float *a,
-                                void *y, float *y32, cudaStream_t st);
-} // namespace fast
+// Router logits (rows skipped when w_router is NULL) into `lg` (lgs floats
+// apart, nrep copies; the shared-gate logit goes to lg[E] of each copy when
+// lgs > 0 and to *sg when sg is non-NULL) and, when xrec is non-NULL, the
+// fixed-point records of x into kRep copies xrs bytes apart.
+cudaError_t launch_router(const Shape &s, const void *x, const void *w_router, const float *bias,
+                          const void *w_sg, float *lg, int lgs, int nrep, float *sg, unsigned char *xrec,
+                          size_t xrs, cudaStream_t st);
+// gate/up SwiGLU then down + weighted combine.
+cudaError_t launch_experts(const Shape &s, const Bufs &b, const ExpertSrc &src, const Routing &R, void *y,
+                           float *y32, cudaStream_t st);
+} // namespace tok
 
 namespace prefill {
 // Calls with at least this many tokens take the grouped-GEMM path.

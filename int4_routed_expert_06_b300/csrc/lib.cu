@@ -2,7 +2,7 @@
 // __device__ variable shared by every kernel, so all sources compile together.
 #include "api.cu"
 #include "kernels_decode.cu"
-#include "kernels_fast.cu"
+#include "kernels_token.cu"
 #include "prefill.cu"
 #include "bucket.cu"
 #include "slot_pool.cu"

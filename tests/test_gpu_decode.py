@@ -175,8 +175,15 @@ def test_route_then_experts_parity(name):
 
 
 def test_fast_and_generic_kernels_agree():
-    """The single-token kernels and the generic ones compute the same layer
-    (different summation order, so within a few fp32 ulps of the output scale)."""
+    """The single-token kernels and the generic ones compute the same layer.
+
+    The single-token kernels carry x and a in 16-bit fixed point per
+    32-column chunk (step = chunk max / 32767, so each element is off by at
+    most 2^-16 of its chunk's largest magnitude) and the generic kernels in
+    fp32.  Those errors are independent across the 2048- and 512-term sums,
+    so the outputs differ by a few 2^-16 of the output scale; the bound below
+    is 2^-11 of it (an order of magnitude of headroom), far inside the
+    oracle tolerance both paths are held to."""
     name = "80b-dec"
     dl = device_layer(name)
     xs = _xs(name, 3)
@@ -188,7 +195,7 @@ def test_fast_and_generic_kernels_agree():
             b = layer_forward(dl, xs[s:s + 1])
             assert torch.equal(a[2], b[2])                      # same routing
             d = (a[1] - b[1]).abs().max().item()
-            assert d <= 1e-5 * max(1.0, b[1].abs().max().item()), d
+            assert d <= 2.0 ** -11 * max(1.0, b[1].abs().max().item()), d
     finally:
         B.moe_set_kernel_path(0)
 
