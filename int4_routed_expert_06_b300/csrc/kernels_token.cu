@@ -1,31 +1,25 @@
 // Single-token (batch-1 decode) path of the routed int4 MoE layer on B300.
 //
-// Three kernels chained with programmatic dependent launch (PDL).  Each kernel
-// lets its successor launch as soon as it starts, loads what does not depend
-// on its predecessor's output (weights, the slot table) before
-// griddepcontrol.wait, and reads its predecessor's outputs and writes its own
-// only after the wait, so a successor never races a kernel that still reads
-// a buffer it is about to overwrite.
+// Two kernels chained with programmatic dependent launch (PDL).  Each kernel
+// loads what does not depend on its predecessor's output (weights, the slot
+// table) before griddepcontrol.wait, and reads its predecessor's outputs and
+// writes its own only after the wait, so a successor never races a kernel
+// that still reads a buffer it is about to overwrite.
 //
-//   router_tok  one warp per router row (E experts, then the shared-gate
-//               row), the row's bf16 weights held in registers before the
-//               wait; after it, x is read and the logits written.  A few
-//               extra CTAs convert x into the fixed-point chunk records the
-//               expert kernels use.
-//   gateup_tok  one CTA per SM.  Before the wait: the CTA's share of the
-//               shared expert's gate/up rows is bulk-copied into shared
-//               memory and the expert->slot table is staged.  After it: top-k
-//               from the logits (one warp per CTA, every CTA), bulk copies of
-//               the CTA's share of the routed rows (one lane per copy, so
-//               they issue in parallel), then a = silu(W_g x) * (W_u x) row
-//               by row as the bytes land.
-//   down_tok    one CTA per SM, owning output rows [h0, h1) of every active
-//               expert.  Before the wait: top-k again and bulk copies of its
-//               rows of every active expert's W_d (they stream while gate/up
-//               runs).  After it: a is converted to fixed-point records in
-//               shared memory and
-//                 y[h] = sum_r w_r (W_d,r a_r)[h] + sigmoid(s) (W_d,sh a_sh)[h]
-//               is accumulated in a fixed order.
+//   router_tok   one warp per router row (E experts, then the shared-gate
+//                row), the row's bf16 weights held in registers before the
+//                wait; after it, x is read and the logits written (in kRep
+//                copies).  A few extra CTAs convert x into the fixed-point
+//                chunk records the expert kernel uses.
+//   experts_tok  one CTA per SM.  Top-k from the logits (one warp per CTA,
+//                every CTA), then every weight byte the CTA needs is copied
+//                into shared memory at once: its 32-row chunks of the active
+//                experts' gate/up rows and its output rows of their W_d.  It
+//                computes a = silu(W_g x) * (W_u x) for its chunks and writes
+//                each chunk's fixed-point record; after a grid-wide barrier it
+//                reads all records and accumulates
+//                  y[h] = sum_r w_r (W_d,r a_r)[h] + sigmoid(s) (W_d,sh a_sh)[h]
+//                for its output rows in a fixed order.
 //
 // Code on the critical path is kept small and loop-shaped: these kernels run
 // once per token on every SM, and long unrolled stretches stall on
@@ -52,13 +46,11 @@ namespace moe {
 namespace tok {
 
 constexpr int kMaxAct = 17;                          // top_k <= 16 plus the shared expert
-constexpr int kMaxSeg = 2;                           // gate/up segments per CTA
-constexpr int kParts = 1;                            // row parts per segment, one barrier each
 constexpr int kMaxE = 1024;                          // experts the staged tables hold
 constexpr uint64_t kWaitNs = 200ull * 1000 * 1000;   // 0.2 s bound on any barrier wait
 constexpr int kRec = 80;                             // bytes per fixed-point chunk record
-constexpr int kGuThreads = 256;
-constexpr int kDnThreads = 512;
+constexpr int kExThreads = 512;
+constexpr int kMaxChunks = 2;                        // 32-row chunks of a per CTA
 
 // ------------------------------------------------------------ PTX helpers
 
@@ -93,14 +85,40 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
                  : "memory");
 }
 
+// 16-byte global -> shared copy through L2 (cp.async); both addresses
+// 16-byte aligned.  Every thread issues its own pieces, so a CTA stages a
+// weight slice without the per-copy setup cost of a bulk copy.
+__device__ __forceinline__ void cp16(void *dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread has issued so far has
+// landed (the barrier's count includes this arrival).
+__device__ __forceinline__ void cp_arrive(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Copy `bytes` (a multiple of 16) cooperatively: thread t of nt takes the
+// 16-byte pieces t, t + nt, ...
+__device__ __forceinline__ void cp_slice(void *dst, const void *src, uint32_t bytes, int t, int nt)
+{
+    for (uint32_t o = (uint32_t)t * 16; o < bytes; o += (uint32_t)nt * 16)
+        cp16(static_cast<char *>(dst) + o, static_cast<const char *>(src) + o);
+}
+
+// One potentially blocking test of the barrier's phase: the thread sleeps
+// until the phase completes or about 1 ms passes (the suspend-time hint), so
+// waiting warps leave the issue slots to the other warps of the SM.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
                  "selp.u32 %0, 1, 0, p;\n\t}"
                  : "=r"(ok)
-                 : "r"(smem_addr(bar)), "r"(parity)
+                 : "r"(smem_addr(bar)), "r"(parity), "r"(1000000u)
                  : "memory");
     return ok != 0;
 }
@@ -171,21 +189,6 @@ __device__ __forceinline__ Chunk load_chunk(const unsigned char *rec)
     return c;
 }
 
-// The same from global memory through L2 (written by an earlier kernel).
-__device__ __forceinline__ Chunk load_chunk_global(const unsigned char *rec)
-{
-    Chunk c;
-    const uint4 *p = reinterpret_cast<const uint4 *>(rec);
-    c.he = __ldcg(p);
-    c.le = __ldcg(p + 1);
-    c.ho = __ldcg(p + 2);
-    c.lo = __ldcg(p + 3);
-    const float2 f = __ldcg(reinterpret_cast<const float2 *>(rec + 64));
-    c.sx = f.x;
-    c.X = f.y;
-    return c;
-}
-
 // Convert 32 values, 4 consecutive ones per lane in each aligned group of 8
 // lanes (lane & 7 = position), into one chunk record, stored at rec and at
 // nrep - 1 further copies `stride` bytes apart.  All 32 lanes call it; lanes
@@ -227,47 +230,6 @@ __device__ __forceinline__ void store_chunk4(const float v[4], unsigned char *re
         h[24 + 2 * m + half] = (unsigned short)(to & 0xFFFFu);
         if (p == 0)
             *reinterpret_cast<float2 *>(rr + 64) = tail;
-    }
-}
-
-// store_chunk4 for U independent groups of values at once (the shuffle
-// chains of the U conversions overlap); rec[u] == nullptr stores nothing.
-template <int U>
-__device__ __forceinline__ void store_chunks4(const float4 (&f)[U], unsigned char *const (&rec)[U], int lane)
-{
-    float am[U], X[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        am[u] = fmaxf(fmaxf(fabsf(f[u].x), fabsf(f[u].y)), fmaxf(fabsf(f[u].z), fabsf(f[u].w)));
-        X[u] = (f[u].x + f[u].y) + (f[u].z + f[u].w);
-    }
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1)
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            am[u] = fmaxf(am[u], __shfl_xor_sync(0xFFFFFFFFu, am[u], o));
-            X[u] += __shfl_xor_sync(0xFFFFFFFFu, X[u], o);
-        }
-    const int p = lane & 7, m = p >> 1, half = p & 1;
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const bool nz = am[u] > 0.f && am[u] < INFINITY;
-        const float inv = nz ? 32767.0f / am[u] : 0.f;
-        const uint32_t f0 = __float_as_uint(fmaf(f[u].x, inv, 12582912.0f));
-        const uint32_t f1 = __float_as_uint(fmaf(f[u].y, inv, 12582912.0f));
-        const uint32_t f2 = __float_as_uint(fmaf(f[u].z, inv, 12582912.0f));
-        const uint32_t f3 = __float_as_uint(fmaf(f[u].w, inv, 12582912.0f));
-        const uint32_t te = __byte_perm(f0, f2, 0x5140);
-        const uint32_t to = __byte_perm(f1, f3, 0x5140);
-        if (rec[u]) {
-            unsigned short *h = reinterpret_cast<unsigned short *>(rec[u]);
-            h[2 * m + half] = (unsigned short)(te >> 16);
-            h[8 + 2 * m + half] = (unsigned short)(te & 0xFFFFu);
-            h[16 + 2 * m + half] = (unsigned short)(to >> 16);
-            h[24 + 2 * m + half] = (unsigned short)(to & 0xFFFFu);
-            if (p == 0)
-                *reinterpret_cast<float2 *>(rec[u] + 64) = make_float2(nz ? am[u] / 32767.0f : 0.f, X[u]);
-        }
     }
 }
 
@@ -489,10 +451,17 @@ __global__ void __launch_bounds__(128) router_tok_kernel(const __nv_bfloat16 *__
                                                         const __nv_bfloat16 *__restrict__ wsg,
                                                         float *__restrict__ lg, int lgs, int nrep,
                                                         float *__restrict__ sg, unsigned char *__restrict__ xrec,
-                                                        size_t xrs, int n_row_ctas)
+                                                        size_t xrs, unsigned int *__restrict__ bar, int n_row_ctas)
 {
     constexpr int H = 256 * NJ;
     pdl_trigger();
+    // the experts kernel that follows counts its CTAs through its grid
+    // barrier from zero (every kernel before this one has completed once the
+    // wait returns, so none still uses the counter)
+    if (bar && blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) {
+        pdl_wait();
+        *bar = 0u;
+    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if ((int)blockIdx.x >= n_row_ctas) {
         // fixed-point records of x: warp v converts chunks 4v .. 4v+3
@@ -543,292 +512,134 @@ __global__ void __launch_bounds__(128) router_tok_kernel(const __nv_bfloat16 *__
         *sg = acc;
 }
 
-// ------------------------------------------------------------ gate/up
+// ------------------------------------------------------------ experts
 
-struct GateUpArgs {
+// One kernel computes the experts of the token: gate/up SwiGLU, then (after a
+// grid-wide barrier) down + weighted combine.
+//
+// Work: a is cut into 32-row chunks, listed as [shared expert's chunks |
+// rank 0's chunks | rank 1's ...]; CTA c takes chunks c and c + gridDim.x.
+// For a chunk it computes the 32 gate and 32 up rows, a = silu(g) u, and the
+// chunk's fixed-point record, which it writes to global memory in kRep
+// copies.  After the barrier every CTA reads all records and computes output
+// rows [h0, h1) of y from its rows of every active expert's W_d.
+//
+// Every weight byte the CTA needs is copied into shared memory right after
+// the routing is known: its chunks' gate and up code rows (bulk copies) and
+// its rows of each active expert's W_d (one bulk copy per expert), plus the
+// scale and bias rows (cp.async by all threads).  Latency-critical reads are
+// kept out of that stream: small reads issued while it is in flight wait
+// behind it.
+struct ExpertsArgs {
     const unsigned char *xrec; // [kRep][xrs] fixed-point records of x
     size_t xrs;
     ExpertSrc src;
     Routing R;
-    float *a;                  // [kRep][as]: [k+1][Imax] each
-    size_t as;
-    int E, k, I, Is, Imax, log2G;
+    unsigned char *arec;       // [kRep][ars]: record of each 32-row chunk of a
+    size_t ars;
+    unsigned int *bar;         // grid barrier counter, zeroed by the router kernel
+    __nv_bfloat16 *y;
+    float *y32;
+    int E, k, I, Is, log2G;
 };
 
-// Rows [o0, o0 + n) of active expert i (i == k: shared) at shared-memory
-// byte offset `off`.
-struct Seg {
-    int i, o0, n;
-    uint32_t off;
-};
-
-// This CTA's rows of the flat list [shared rows | rank 0 rows | rank 1 ...],
-// as at most kMaxSeg segments (the host checks that a share is no longer
-// than the shortest expert, so it crosses at most one boundary).
-__device__ __forceinline__ int gateup_segments(int c, int n, int k, int I, int Is, uint32_t rowpair, Seg *seg)
+// Chunk j of the list: active expert *i (k = shared) and its first row *o0.
+__device__ __forceinline__ void chunk_of(int j, int k, int I, int Is, int *i, int *o0)
 {
-    const long R = (long)Is + (long)k * I;
-    int r = (int)((long)c * R / n);
-    const int r1 = (int)((long)(c + 1) * R / n);
-    int ns = 0;
-    uint32_t off = 0;
-    while (r < r1 && ns < kMaxSeg) {
-        int i, o, len;
-        if (r < Is) {
-            i = k;
-            o = r;
-            len = min(r1, Is) - r;
-        } else {
-            i = (r - Is) / I;
-            o = (r - Is) - i * I;
-            len = min(r1 - r, I - o);
-        }
-        seg[ns++] = Seg{i, o, len, off};
-        off += (uint32_t)len * rowpair;
-        r += len;
+    const int ns = Is >> 5;
+    if (j < ns) {
+        *i = k;
+        *o0 = 32 * j;
+    } else {
+        const int r = (j - ns) / (I >> 5);
+        *i = r;
+        *o0 = 32 * ((j - ns) - r * (I >> 5));
     }
-    return ns;
 }
 
-// Part p of a segment of n rows: rows [p n / kParts, (p+1) n / kParts); the
-// part of row r is floor(((r + 1) kParts - 1) / n).
-__device__ __forceinline__ int part_begin(int n, int p) { return p * n / kParts; }
-__device__ __forceinline__ int part_of(int n, int r) { return ((r + 1) * kParts - 1) / n; }
+// Index in the list of chunk ch of active expert i.
+__device__ __forceinline__ int chunk_index(int i, int ch, int k, int I, int Is)
+{
+    return i == k ? ch : (Is >> 5) + i * (I >> 5) + ch;
+}
 
-// H = 1024 * NXC; TS = scale/bias type.  One CTA per SM.
+__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int *p)
+{
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// H = 1024 * NXC; TS = scale/bias type.  One CTA of kExThreads per SM.
 //
-// Shared memory: the segments' rows (codes of gate, codes of up, then the
-// four scale/bias arrays, per segment).  Each segment arrives in kParts row
-// parts, each completing on its own barrier, so rows are computed while the
-// rest of the share streams in.  Lane l takes chunks NXC l .. NXC l + NXC - 1
-// of a row; a warp computes two rows per pass.
+// Shared memory (dynamic): per chunk [64 code rows (32 gate, then 32 up)]
+// [64 scale rows][64 bias rows]; then per active expert its down rows (codes
+// [nr][I_i/2], scales and biases [nr][I_i/G] each); then the records of a.
 template <int NXC, typename TS>
-__global__ void __launch_bounds__(kGuThreads, 2) gateup_tok_kernel(GateUpArgs A)
+__global__ void __launch_bounds__(kExThreads, 1) experts_tok_kernel(ExpertsArgs A)
 {
     constexpr int H = 1024 * NXC;
-    constexpr int NW = kGuThreads / 32;
-    constexpr int XQ = (H / 32) * kRec / 16; // 16-byte pieces of the x records
-    constexpr int XU = (XQ + kGuThreads - 33) / (kGuThreads - 32);
+    constexpr int NW = kExThreads / 32;
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ uint64_t bars[kMaxSeg][kParts];
+    __shared__ uint64_t cbar[kMaxChunks], dbar, xbar;
     __shared__ int tab[kMaxE];
     __shared__ __align__(16) unsigned char xs[(H / 32) * kRec];
     __shared__ int s_idx[kMaxAct];
-    __shared__ float s_w[kMaxAct];
-    __shared__ const char *s_base[kMaxSeg];
-    __shared__ __align__(16) TopkSmem tks;
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n = gridDim.x, c = blockIdx.x, rep = c % kRep;
-    const int k = A.k;
-    const int HG = H >> A.log2G;                     // groups per row
-    const uint32_t qrow = H / 2;                     // code bytes per row
-    const uint32_t srow = (uint32_t)HG * sizeof(TS); // scale (or bias) bytes per row
-    const uint32_t rowpair = 2 * qrow + 4 * srow;
-
-    Seg seg[kMaxSeg];
-    const int nseg = gateup_segments(c, n, k, A.I, A.Is, rowpair, seg);
-
-    // Copy m (0..5: gate codes, up codes, gate scales, gate biases, up
-    // scales, up biases) of part p of segment s.
-    auto issue = [&](int s, int p, int m, const char *base) {
-        const Seg &g = seg[s];
-        const int r0 = part_begin(g.n, p), nrow = part_begin(g.n, p + 1) - r0;
-        if (nrow <= 0)
-            return;
-        const size_t *offs = (g.i == k) ? A.src.off_sh : A.src.off;
-        const uint32_t n_q = (uint32_t)g.n * qrow, n_s = (uint32_t)g.n * srow;
-        const int mat = m == 0 ? M_QG : m == 1 ? M_QU : m == 2 ? M_SG : m == 3 ? M_BG : m == 4 ? M_SU : M_BU;
-        const uint32_t rb = m < 2 ? qrow : srow;
-        const uint32_t doff = (m < 2 ? (uint32_t)m * n_q : 2 * n_q + (uint32_t)(m - 2) * n_s) + (uint32_t)r0 * rb;
-        bulk_g2s(smem + g.off + doff, base + offs[mat] + (size_t)(g.o0 + r0) * rb, (uint32_t)nrow * rb, &bars[s][p]);
-    };
-    auto arm = [&](int s, int p, bool full) {
-        const int nrow = part_begin(seg[s].n, p + 1) - part_begin(seg[s].n, p);
-        if (nrow > 0)
-            mbar_expect_tx(&bars[s][p], full ? (uint32_t)nrow * rowpair : 0u);
-    };
-
-    // ---- before the wait: nothing here depends on the router's output
-    const bool sh0 = nseg > 0 && seg[0].i == k;
-    if (warp == 0) {
-        if (lane == 0) {
-            for (int s = 0; s < kMaxSeg; ++s)
-                for (int p = 0; p < kParts; ++p)
-                    mbar_init(&bars[s][p], 1);
-            fence_mbar_init();
-            if (sh0) {
-                s_base[0] = A.src.shared;
-                for (int p = 0; p < kParts; ++p)
-                    arm(0, p, true);
-            }
-        }
-        __syncwarp();
-        if (sh0 && lane < 6 * kParts)
-            issue(0, lane / 6, lane % 6, A.src.shared);
-    }
-    for (int e = threadIdx.x; e < A.E; e += kGuThreads)
-        tab[e] = __ldg(A.src.table + e);
-    __syncthreads();
-
-    // ---- after the wait: warp 0 selects the top k and issues the routed
-    // copies, the other warps stage the x records meanwhile
-    pdl_wait();
-    if (warp == 0) {
-        load_routing(A.R, rep, A.E, k, lane, s_idx, s_w, tks, c == 0);
-        // lane s kParts + p arms part p of segment s
-        const int ls = lane / kParts, lp = lane % kParts;
-        const char *b = nullptr;
-        if (ls < nseg && seg[ls].i != k) {
-            b = routed_base(A.src, tab, s_idx[seg[ls].i]);
-            if (lp == 0)
-                s_base[ls] = b;
-            arm(ls, lp, b != nullptr);
-        }
-        __syncwarp();
-        // copy q = lane + 32 t is copy q % 6 of part (q / 6) % kParts of segment q / (6 kParts)
-        for (int q = lane; q < 6 * kParts * nseg; q += 32) {
-            const int s = q / (6 * kParts), p = (q / 6) % kParts, m = q % 6;
-            if (seg[s].i != k && s_base[s])
-                issue(s, p, m, s_base[s]);
-        }
-    } else {
-        const uint4 *src = reinterpret_cast<const uint4 *>(A.xrec + (size_t)rep * A.xrs);
-        uint4 *dst = reinterpret_cast<uint4 *>(xs);
-        uint4 v[XU];
-#pragma unroll
-        for (int u = 0; u < XU; ++u) {
-            const int q = threadIdx.x - 32 + u * (kGuThreads - 32);
-            if (q < XQ)
-                v[u] = __ldcg(src + q);
-        }
-#pragma unroll
-        for (int u = 0; u < XU; ++u) {
-            const int q = threadIdx.x - 32 + u * (kGuThreads - 32);
-            if (q < XQ)
-                dst[q] = v[u];
-        }
-    }
-    __syncthreads();
-    // down may launch now: its prologue (its own top-k and weight copies)
-    // would otherwise compete with the routed copies issued above
-    pdl_trigger();
-
-    Chunk xv[NXC];
-#pragma unroll
-    for (int m = 0; m < NXC; ++m)
-        xv[m] = load_chunk(xs + (size_t)(NXC * lane + m) * kRec);
-    int grp[NXC];
-#pragma unroll
-    for (int m = 0; m < NXC; ++m)
-        grp[m] = ((NXC * lane + m) * 32) >> A.log2G;
-
-    const int total = nseg == 0 ? 0 : (int)(seg[nseg - 1].off / rowpair) + seg[nseg - 1].n;
-    uint32_t waited = 0; // bit s * kParts + p: part p of segment s has landed
-#pragma unroll 1
-    for (int rho0 = warp; rho0 < total; rho0 += 2 * NW) {
-        float gacc[2] = {0.f, 0.f}, uacc[2] = {0.f, 0.f};
-        float *dst[2] = {nullptr, nullptr};
-        bool ok = true;
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            const int rho = rho0 + t * NW;
-            if (rho >= total)
-                continue;
-            int s = 0, r = rho;
-            if (nseg > 1 && r >= seg[0].n) {
-                r -= seg[0].n;
-                s = 1;
-            }
-            const Seg &g = seg[s];
-            const uint32_t bit = 1u << (s * kParts + part_of(g.n, r));
-            if (!(waited & bit)) {
-                // warp-uniform outcome, so no lane leaves the shuffles below
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait0(&bars[s][part_of(g.n, r)]))) {
-                    ok = false;
-                    continue;
-                }
-                waited |= bit;
-            }
-            dst[t] = A.a + (size_t)g.i * A.Imax + g.o0 + r;
-            if (s_base[s] == nullptr)
-                continue;
-            const uint32_t n_q = (uint32_t)g.n * qrow, n_s = (uint32_t)g.n * srow;
-            const unsigned char *d = smem + g.off;
-            const uint4 *qg = reinterpret_cast<const uint4 *>(d + (size_t)r * qrow);
-            const uint4 *qu = reinterpret_cast<const uint4 *>(d + n_q + (size_t)r * qrow);
-            const TS *sg = reinterpret_cast<const TS *>(d + 2 * n_q) + (size_t)r * HG;
-            const TS *bg = reinterpret_cast<const TS *>(d + 2 * n_q + n_s) + (size_t)r * HG;
-            const TS *su = reinterpret_cast<const TS *>(d + 2 * n_q + 2 * n_s) + (size_t)r * HG;
-            const TS *bu = reinterpret_cast<const TS *>(d + 2 * n_q + 3 * n_s) + (size_t)r * HG;
-#pragma unroll
-            for (int m = 0; m < NXC; ++m) {
-                const int ch = NXC * lane + m;
-                gacc[t] += chunk_term(qg[ch], xv[m], ld_sb(sg + grp[m]), ld_sb(bg + grp[m]));
-                uacc[t] += chunk_term(qu[ch], xv[m], ld_sb(su + grp[m]), ld_sb(bu + grp[m]));
-            }
-        }
-        if (!ok)
-            return;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            gacc[0] += __shfl_xor_sync(0xFFFFFFFFu, gacc[0], o);
-            uacc[0] += __shfl_xor_sync(0xFFFFFFFFu, uacc[0], o);
-            gacc[1] += __shfl_xor_sync(0xFFFFFFFFu, gacc[1], o);
-            uacc[1] += __shfl_xor_sync(0xFFFFFFFFu, uacc[1], o);
-        }
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-            if (dst[t] && lane < kRep)
-                dst[t][(size_t)lane * A.as] = gacc[t] * sigmoid_f(gacc[t]) * uacc[t];
-    }
-}
-
-// ------------------------------------------------------------ down + combine
-
-struct DownArgs {
-    ExpertSrc src;
-    Routing R;
-    const float *a;         // [kRep][as]: [k+1][Imax] each
-    size_t as;
-    __nv_bfloat16 *y;
-    float *y32;
-    int E, H, k, I, Is, Imax, log2G, n_act;
-};
-
-// CTA c owns output rows [h0, h1), nr = h1 - h0 <= 16.  Shared memory: per
-// active expert i its rows' codes [nr][I_i/2], scales and biases
-// [nr][I_i/G] each; then the fixed-point records of a, [n_act][Imax/32].
-//
-// Warp w computes output row w: lane l & 15 takes chunks l, l+16, ... of the
-// row for the experts of parity l >> 4 (rank order, shared expert last), and
-// the warp sums its lanes in a fixed tree, so the order of the sum does not
-// depend on where the experts live.
-template <typename TS>
-__global__ void __launch_bounds__(kDnThreads, 2) down_tok_kernel(DownArgs A)
-{
-    constexpr int kBatch = 4; // float4 loads of a in flight per thread
-    extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ uint64_t bar;
-    __shared__ int s_idx[kMaxAct];
     __shared__ float s_w[kMaxAct + 1];
-    __shared__ const char *s_base[kMaxAct];
-    __shared__ uint32_t s_eoff[kMaxAct + 1]; // shared-memory offset of expert i's rows
-    __shared__ int s_qb[kMaxAct];            // code bytes per row of expert i
-    __shared__ int s_ng[kMaxAct];            // groups per row of expert i
+    __shared__ const char *s_base[kMaxAct];  // blob of active expert i (i == k: shared), or nullptr
+    __shared__ uint32_t s_eoff[kMaxAct + 1]; // offset of expert i's down rows in the down region
+    __shared__ int s_qb[kMaxAct];            // down code bytes per row of expert i
+    __shared__ int s_ng[kMaxAct];            // down groups per row of expert i
+    __shared__ __align__(16) float s_a[kMaxChunks][32]; // read as float4
     __shared__ __align__(16) TopkSmem tks;
 
-    pdl_trigger(); // the next layer call may start its own weight loads now
-
-    const int n = gridDim.x, c = blockIdx.x, rep = c % kRep;
-    const int h0 = (int)((long)c * A.H / n), h1 = (int)((long)(c + 1) * A.H / n);
-    const int nr = h1 - h0;
-    const int k = A.k, n_act = A.n_act;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n = gridDim.x, c = blockIdx.x, rep = c % kRep;
+    const int k = A.k, n_act = k + 1;
+    const int HG = H >> A.log2G;                     // groups per gate/up row
+    const uint32_t qrow = H / 2;                     // code bytes per gate/up row
+    const uint32_t srow = (uint32_t)HG * sizeof(TS); // scale (or bias) bytes per gate/up row
+    const uint32_t cbytes = 64 * (qrow + 2 * srow);  // one chunk in shared memory
     const uint32_t sb = sizeof(TS);
+    const int NC = (A.Is >> 5) + k * (A.I >> 5);
+    int nch = 0, cj[kMaxChunks];
+    for (int j = c; j < NC && nch < kMaxChunks; j += n)
+        cj[nch++] = j;
+    const int h0 = (int)((long)c * (long)H / n), h1 = (int)((long)(c + 1) * (long)H / n);
+    const int nr = h1 - h0;
+    unsigned char *down = smem + nch * cbytes;
 
+    // Chunk s: thread `lead` arms its barrier and bulk-copies the 32 gate and
+    // 32 up code rows; every thread cp.asyncs its pieces of the scale and
+    // bias rows and arrives.
+    auto stage_chunk = [&](int s, const char *b, bool lead) {
+        int i, o0;
+        chunk_of(cj[s], k, A.I, A.Is, &i, &o0);
+        const size_t *offs = (i == k) ? A.src.off_sh : A.src.off;
+        unsigned char *d = smem + s * cbytes;
+        if (lead) {
+            mbar_expect_tx(&cbar[s], b ? 64 * qrow : 0u);
+            if (b) {
+                bulk_g2s(d, b + offs[M_QG] + (size_t)o0 * qrow, 32 * qrow, &cbar[s]);
+                bulk_g2s(d + 32 * qrow, b + offs[M_QU] + (size_t)o0 * qrow, 32 * qrow, &cbar[s]);
+            }
+        }
+        if (b) {
+            unsigned char *ds = d + 64 * qrow;
+            cp_slice(ds, b + offs[M_SG] + (size_t)o0 * srow, 32 * srow, threadIdx.x, kExThreads);
+            cp_slice(ds + 32 * srow, b + offs[M_SU] + (size_t)o0 * srow, 32 * srow, threadIdx.x, kExThreads);
+            cp_slice(ds + 64 * srow, b + offs[M_BG] + (size_t)o0 * srow, 32 * srow, threadIdx.x, kExThreads);
+            cp_slice(ds + 96 * srow, b + offs[M_BU] + (size_t)o0 * srow, 32 * srow, threadIdx.x, kExThreads);
+        }
+        cp_arrive(&cbar[s]);
+    };
+
+    // ---- before the wait: only what does not depend on the router's output
     if (threadIdx.x == 0) {
-        mbar_init(&bar, 1);
+        for (int s = 0; s < kMaxChunks; ++s)
+            mbar_init(&cbar[s], kExThreads + 1);
+        mbar_init(&dbar, kExThreads + 1);
+        mbar_init(&xbar, kExThreads);
         fence_mbar_init();
         uint32_t o = 0;
         for (int i = 0; i < n_act; ++i) {
@@ -839,66 +650,141 @@ __global__ void __launch_bounds__(kDnThreads, 2) down_tok_kernel(DownArgs A)
             o += (uint32_t)nr * ((uint32_t)inter / 2 + 2 * (uint32_t)(inter >> A.log2G) * sb);
         }
         s_eoff[n_act] = o;
-        s_w[kMaxAct] = sigmoid_f(__ldcg(A.R.logits ? A.R.logits + (size_t)rep * A.R.lgs + A.E : A.R.sg_logit));
+        s_base[k] = A.src.shared;
     }
+    for (int e = threadIdx.x; e < A.E; e += kExThreads)
+        tab[e] = __ldg(A.src.table + e);
     __syncthreads();
-    if (warp == 0) {
-        load_routing(A.R, rep, A.E, k, lane, s_idx, s_w, tks, false);
-        const char *b = nullptr;
-        uint32_t bytes = 0;
-        if (lane < n_act) {
-            b = lane == k ? A.src.shared : routed_base(A.src, A.src.table, s_idx[lane]);
-            s_base[lane] = b;
-            if (b)
-                bytes = s_eoff[lane + 1] - s_eoff[lane];
-        }
-        const uint32_t tot = __reduce_add_sync(0xFFFFFFFFu, bytes);
-        if (lane == 0)
-            mbar_expect_tx(&bar, tot);
-        __syncwarp();
-        if (b) {
-            const size_t *offs = (lane == k) ? A.src.off_sh : A.src.off;
-            const uint32_t nq = (uint32_t)nr * s_qb[lane], ns = (uint32_t)nr * s_ng[lane] * sb;
-            unsigned char *d = smem + s_eoff[lane];
-            bulk_g2s(d, b + offs[M_QD] + (size_t)h0 * s_qb[lane], nq, &bar);
-            bulk_g2s(d + nq, b + offs[M_SD] + (size_t)h0 * s_ng[lane] * sb, ns, &bar);
-            bulk_g2s(d + nq + ns, b + offs[M_BD] + (size_t)h0 * s_ng[lane] * sb, ns, &bar);
-        }
-    }
-    __syncthreads();
-    unsigned char *arec = smem + ((s_eoff[n_act] + 15) & ~15u); // [n_act][nchm] records
-    const int nchm = A.Imax >> 5;
+    // the shared expert's chunks come first in the list: stage them now
+    for (int s = 0; s < nch; ++s)
+        if (cj[s] < (A.Is >> 5))
+            stage_chunk(s, A.src.shared, threadIdx.x == 32 * s);
 
+    // ---- after the wait: x records and the shared-gate logit are fetched
+    // while warp 0 selects the top k; then every copy is issued
     pdl_wait();
-    // a -> fixed-point records; 8 lanes per 32-value chunk, kBatch loads in
-    // flight per thread before any conversion
-    {
-        const int n4 = n_act * A.Imax / 4;
-        const float4 *a4 = reinterpret_cast<const float4 *>(A.a + (size_t)rep * A.as);
-#pragma unroll 1
-        for (int q0 = 0; q0 < n4; q0 += kBatch * kDnThreads) {
-            float4 f[kBatch];
-            unsigned char *rec[kBatch];
+    cp_slice(xs, A.xrec + (size_t)rep * A.xrs, (H / 32) * kRec, threadIdx.x, kExThreads);
+    cp_arrive(&xbar);
+    if (threadIdx.x == 32)
+        s_w[kMaxAct] = sigmoid_f(__ldcg(A.R.logits ? A.R.logits + (size_t)rep * A.R.lgs + A.E : A.R.sg_logit));
+    if (warp == 0) {
+        load_routing(A.R, rep, A.E, k, lane, s_idx, s_w, tks, c == 0);
+        if (lane < k)
+            s_base[lane] = routed_base(A.src, tab, s_idx[lane]);
+    }
+    __syncthreads();
+    for (int s = 0; s < nch; ++s)
+        if (cj[s] >= (A.Is >> 5)) {
+            int i, o0;
+            chunk_of(cj[s], k, A.I, A.Is, &i, &o0);
+            stage_chunk(s, s_base[i], threadIdx.x == 32 * s);
+        }
+    // down rows: lane i of warp 2 bulk-copies expert i's code rows, lane 0
+    // arms the barrier; every thread stages scale and bias rows
+    if (warp == 2) {
+        const char *b = lane < n_act ? s_base[lane] : nullptr;
+        const uint32_t nq = b ? (uint32_t)nr * s_qb[lane] : 0u;
+        const uint32_t tot = __reduce_add_sync(0xFFFFFFFFu, nq);
+        if (lane == 0)
+            mbar_expect_tx(&dbar, tot);
+        __syncwarp();
+        if (b && nq)
+            bulk_g2s(down + s_eoff[lane], b + (lane == k ? A.src.off_sh : A.src.off)[M_QD] + (size_t)h0 * s_qb[lane],
+                     nq, &dbar);
+    }
+    for (int i = 0; i < n_act; ++i) {
+        const char *b = s_base[i];
+        if (!b)
+            continue;
+        const size_t *offs = (i == k) ? A.src.off_sh : A.src.off;
+        const uint32_t nq = (uint32_t)nr * s_qb[i], ns = (uint32_t)nr * s_ng[i] * sb;
+        unsigned char *d = down + s_eoff[i];
+        cp_slice(d + nq, b + offs[M_SD] + (size_t)h0 * s_ng[i] * sb, ns, threadIdx.x, kExThreads);
+        cp_slice(d + nq + ns, b + offs[M_BD] + (size_t)h0 * s_ng[i] * sb, ns, threadIdx.x, kExThreads);
+    }
+    cp_arrive(&dbar);
+
+    // ---- gate/up: warp w computes row pairs w and w + 16 of each chunk
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait0(&xbar)))
+        return;
+    Chunk xv[NXC];
+    int grp[NXC];
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int q = q0 + u * kDnThreads + threadIdx.x;
-                f[u] = q < n4 ? __ldcg(a4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
-                // chunk q >> 3 == (i * Imax + col) / 32 == i * nchm + col / 32
-                rec[u] = q < n4 ? arec + (size_t)(q >> 3) * kRec : nullptr;
+    for (int m = 0; m < NXC; ++m) {
+        xv[m] = load_chunk(xs + (size_t)(NXC * lane + m) * kRec);
+        grp[m] = ((NXC * lane + m) * 32) >> A.log2G;
+    }
+    for (int s = 0; s < nch; ++s) {
+        int i, o0;
+        chunk_of(cj[s], k, A.I, A.Is, &i, &o0);
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait0(&cbar[s])))
+            return;
+        const unsigned char *d = smem + s * cbytes;
+        const TS *sc = reinterpret_cast<const TS *>(d + 64 * qrow);
+        const TS *bi = sc + 64 * HG;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f}; // gate t0, up t0, gate t1, up t1
+        if (s_base[i]) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const int row = (v & 1) * 32 + warp + (v >> 1) * NW; // smem row of this gate/up row
+                const uint4 *q = reinterpret_cast<const uint4 *>(d + (size_t)row * qrow);
+#pragma unroll
+                for (int m = 0; m < NXC; ++m)
+                    acc[v] += chunk_term(q[NXC * lane + m], xv[m], ld_sb(sc + row * HG + grp[m]),
+                                         ld_sb(bi + row * HG + grp[m]));
             }
-            store_chunks4<kBatch>(f, rec, lane);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+                acc[v] += __shfl_xor_sync(0xFFFFFFFFu, acc[v], o);
+        if (lane == 0) {
+            s_a[s][warp] = acc[0] * sigmoid_f(acc[0]) * acc[1];
+            s_a[s][warp + NW] = acc[2] * sigmoid_f(acc[2]) * acc[3];
         }
     }
     __syncthreads();
-    const bool ready = mbar_wait0(&bar);
+    // chunk records: warp s, lanes 0..7, four values each
+    if (warp < nch) {
+        const float4 v = *reinterpret_cast<const float4 *>(&s_a[warp][4 * (lane & 7)]);
+        const float f[4] = {v.x, v.y, v.z, v.w};
+        store_chunk4(f, A.arec + (size_t)cj[warp] * kRec, lane, lane < 8, kRep, A.ars);
+    }
 
+    // ---- grid barrier: every chunk record is written
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(A.bar, 1u);
+        const uint64_t t0 = global_ns();
+        while (ld_acquire_u32(A.bar) < (unsigned int)n) {
+            if (global_ns() - t0 > kWaitNs) {
+                record_error(MOE_ERR_TIMEOUT);
+                break;
+            }
+        }
+    }
+    __syncthreads();
+    pdl_trigger(); // the next layer call may start its own weight loads now
+    unsigned char *arec = down + ((s_eoff[n_act] + 15) & ~15u);
+    {
+        const uint4 *src = reinterpret_cast<const uint4 *>(A.arec + (size_t)rep * A.ars);
+        uint4 *dst = reinterpret_cast<uint4 *>(arec);
+        for (int q = threadIdx.x; q < NC * kRec / 16; q += kExThreads)
+            dst[q] = __ldcg(src + q);
+    }
+    __syncthreads();
+    const bool ready = __all_sync(0xFFFFFFFFu, mbar_wait0(&dbar));
+
+    // ---- down: warp w computes output row w; lane l & 15 takes chunks l,
+    // l+16, ... of the row for the experts of parity l >> 4 (rank order,
+    // shared last), two experts at a time; the warp sums its lanes in a
+    // fixed tree, so the order does not depend on where the experts live
     const int par = lane >> 4, l16 = lane & 15;
     const int hr = warp;
     float acc = 0.f;
     if (ready && hr < nr) {
-        // experts par, par + 2, ... two at a time; every chunk's loads are
-        // issued before any of its dot products.  Both half-warps run the
-        // same number of passes (the warp-wide vote below needs every lane).
         constexpr int U = 2;
 #pragma unroll 1
         for (int i0 = 0; i0 < n_act; i0 += 2 * U) {
@@ -916,11 +802,11 @@ __global__ void __launch_bounds__(kDnThreads, 2) down_tok_kernel(DownArgs A)
                     const bool live = i < n_act && s_base[ic] != nullptr && ch < (qb >> 4);
                     any |= ch0 < (qb >> 4) && i < n_act;
                     const int chc = live ? ch : 0;
-                    const unsigned char *d = smem + s_eoff[ic];
+                    const unsigned char *d = down + s_eoff[ic];
                     const TS *sd = reinterpret_cast<const TS *>(d + nr * qb) + hr * ng;
                     const int g = (chc * 32) >> A.log2G;
                     q[u] = reinterpret_cast<const uint4 *>(d + hr * qb)[chc];
-                    av[u] = load_chunk(arec + (size_t)(ic * nchm + chc) * kRec);
+                    av[u] = load_chunk(arec + (size_t)chunk_index(ic, chc, k, A.I, A.Is) * kRec);
                     sc[u] = ld_sb(sd + g);
                     bc[u] = ld_sb(sd + nr * ng + g);
                     wi[u] = live ? ((i < k) ? s_w[i] : s_w[kMaxAct]) : 0.f;
@@ -982,30 +868,29 @@ static int log2i(int v)
     return l;
 }
 
-static size_t gateup_smem(const Shape &s, int n)
+// Dynamic shared memory of the experts kernel for a CTA with `nch` chunks.
+static size_t experts_smem(const Shape &s, int n, int nch)
 {
     const size_t sb = s.qscale == MOE_F16 ? 2 : 4;
-    const size_t rowpair = (size_t)s.H + 4 * (size_t)(s.H / s.G) * sb;
-    const long R = (long)s.Is + (long)s.k * s.I;
-    return (size_t)((R + n - 1) / n) * rowpair;
-}
-
-static size_t down_smem(const Shape &s, int n)
-{
-    const size_t sb = s.qscale == MOE_F16 ? 2 : 4;
+    const size_t chunk = 64 * ((size_t)s.H / 2 + 2 * (size_t)(s.H / s.G) * sb);
     const int nr = (s.H + n - 1) / n;
-    const int n_act = s.k + 1;
-    const int imax = s.I > s.Is ? s.I : s.Is;
     size_t w = 0;
-    for (int i = 0; i < n_act; ++i) {
+    for (int i = 0; i <= s.k; ++i) {
         const int inter = (i == s.k) ? s.Is : s.I;
         w += (size_t)nr * (inter / 2 + 2 * (inter / s.G) * sb);
     }
     w = (w + 15) & ~(size_t)15;
-    return w + (size_t)kRec * n_act * (imax / 32);
+    const int NC = s.Is / 32 + s.k * (s.I / 32);
+    return nch * chunk + w + (size_t)kRec * NC;
 }
 
-constexpr size_t kSmemBudget = 100 * 1024; // a gate/up and a down CTA share an SM
+static int max_chunks(const Shape &s, int n)
+{
+    const int NC = s.Is / 32 + s.k * (s.I / 32);
+    return (NC + n - 1) / n;
+}
+
+constexpr size_t kSmemLimit = 220 * 1024;
 
 bool eligible(const Shape &s)
 {
@@ -1023,13 +908,11 @@ bool eligible(const Shape &s)
     if (s.I % 32 || s.Is % 32 || s.G < 32)
         return false;
     const int n = sm_count();
-    const long R = (long)s.Is + (long)s.k * s.I;
-    const long share = (R + n - 1) / n;
-    if (share > s.I || share > s.Is) // a CTA's gate/up share crosses at most one expert boundary
+    if (max_chunks(s, n) > kMaxChunks)        // a CTA owns at most kMaxChunks chunks of a
         return false;
-    if ((s.H + n - 1) / n > kDnThreads / 32) // down: one output row per warp
+    if ((s.H + n - 1) / n > kExThreads / 32)  // down: one output row per warp
         return false;
-    return gateup_smem(s, n) <= kSmemBudget && down_smem(s, n) <= kSmemBudget;
+    return experts_smem(s, n, max_chunks(s, n)) <= kSmemLimit;
 }
 
 // All three kernels run with the same (maximal) shared-memory carveout: an SM
@@ -1050,31 +933,33 @@ static size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 size_t bufs_bytes(const Shape &s)
 {
-    const int imax = s.I > s.Is ? s.I : s.Is;
+    const int NC = s.Is / 32 + s.k * (s.I / 32);
     const size_t lg = up256(sizeof(float) * (size_t)(s.E + 1));
     const size_t xr = up256((size_t)kRec * (s.H / 32));
-    const size_t a = up256(sizeof(float) * (size_t)(s.k + 1) * imax);
-    return kRep * (lg + xr + a);
+    const size_t ar = up256((size_t)kRec * NC);
+    return kRep * (lg + xr + ar) + 256;
 }
 
 Bufs bufs_carve(const Shape &s, char *base)
 {
-    const int imax = s.I > s.Is ? s.I : s.Is;
+    const int NC = s.Is / 32 + s.k * (s.I / 32);
     const size_t lg = up256(sizeof(float) * (size_t)(s.E + 1));
     const size_t xr = up256((size_t)kRec * (s.H / 32));
-    const size_t a = up256(sizeof(float) * (size_t)(s.k + 1) * imax);
+    const size_t ar = up256((size_t)kRec * NC);
     Bufs b;
     b.lg = reinterpret_cast<float *>(base);
     b.lgs = (int)(lg / sizeof(float));
     b.xrec = reinterpret_cast<unsigned char *>(base + kRep * lg);
     b.xrs = xr;
-    b.a = reinterpret_cast<float *>(base + kRep * (lg + xr));
-    b.as = a / sizeof(float);
+    b.arec = reinterpret_cast<unsigned char *>(base + kRep * (lg + xr));
+    b.ars = ar;
+    b.bar = reinterpret_cast<unsigned int *>(base + kRep * (lg + xr + ar));
     return b;
 }
 
 cudaError_t launch_router(const Shape &s, const void *x, const void *w_router, const float *bias, const void *w_sg,
-                          float *lg, int lgs, int nrep, float *sg, unsigned char *xrec, size_t xrs, cudaStream_t st)
+                          float *lg, int lgs, int nrep, float *sg, unsigned char *xrec, size_t xrs, unsigned int *bar,
+                          cudaStream_t st)
 {
     const int rows = w_router ? s.E + (w_sg ? 1 : 0) : 0;
     const int row_ctas = (rows + 3) / 4;
@@ -1090,62 +975,38 @@ cudaError_t launch_router(const Shape &s, const void *x, const void *w_router, c
         e = set_carveout(router_tok_kernel<4>, &cv4);
         return e != cudaSuccess ? e
                                 : launch_pdl(router_tok_kernel<4>, grid, 128, 0, st, xb, s.E, wr, bias, ws, lg, lgs,
-                                             nrep, sg, xrec, xrs, row_ctas);
+                                             nrep, sg, xrec, xrs, bar, row_ctas);
     }
     e = set_carveout(router_tok_kernel<8>, &cv8);
     return e != cudaSuccess ? e
                             : launch_pdl(router_tok_kernel<8>, grid, 128, 0, st, xb, s.E, wr, bias, ws, lg, lgs, nrep,
-                                         sg, xrec, xrs, row_ctas);
+                                         sg, xrec, xrs, bar, row_ctas);
 }
 
 template <int NXC, typename TS>
-static cudaError_t gateup_go(const GateUpArgs &A, int n, size_t smem, cudaStream_t st)
+static cudaError_t experts_go(const ExpertsArgs &A, int n, size_t smem, cudaStream_t st)
 {
     static int cur = 0;
     static bool cv = false;
-    cudaError_t e = set_carveout(gateup_tok_kernel<NXC, TS>, &cv);
+    cudaError_t e = set_carveout(experts_tok_kernel<NXC, TS>, &cv);
     if (e == cudaSuccess)
-        e = ensure_smem(gateup_tok_kernel<NXC, TS>, smem, &cur);
+        e = ensure_smem(experts_tok_kernel<NXC, TS>, smem, &cur);
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(gateup_tok_kernel<NXC, TS>, n, kGuThreads, smem, st, A);
-}
-
-template <typename TS>
-static cudaError_t down_go(const DownArgs &A, int n, size_t smem, cudaStream_t st)
-{
-    static int cur = 0;
-    static bool cv = false;
-    cudaError_t e = set_carveout(down_tok_kernel<TS>, &cv);
-    if (e == cudaSuccess)
-        e = ensure_smem(down_tok_kernel<TS>, smem, &cur);
-    if (e != cudaSuccess)
-        return e;
-    return launch_pdl(down_tok_kernel<TS>, n, kDnThreads, smem, st, A);
+    return launch_pdl(experts_tok_kernel<NXC, TS>, n, kExThreads, smem, st, A);
 }
 
 cudaError_t launch_experts(const Shape &s, const Bufs &b, const ExpertSrc &src, const Routing &R, void *y,
                            float *y32, cudaStream_t st)
 {
     const int n = sm_count();
-    const int imax = s.I > s.Is ? s.I : s.Is;
-    const int lg = log2i(s.G);
-    GateUpArgs g{b.xrec, b.xrs, src, R, b.a, b.as, s.E, s.k, s.I, s.Is, imax, lg};
-    const size_t gs = gateup_smem(s, n);
+    ExpertsArgs A{b.xrec, b.xrs, src, R, b.arec, b.ars, b.bar, static_cast<__nv_bfloat16 *>(y), y32,
+                  s.E, s.k, s.I, s.Is, log2i(s.G)};
+    const size_t smem = experts_smem(s, n, max_chunks(s, n));
     const bool f16 = s.qscale == MOE_F16;
-    cudaError_t e;
     if (s.H == 1024)
-        e = f16 ? gateup_go<1, __half>(g, n, gs, st) : gateup_go<1, float>(g, n, gs, st);
-    else
-        e = f16 ? gateup_go<2, __half>(g, n, gs, st) : gateup_go<2, float>(g, n, gs, st);
-    if (e != cudaSuccess)
-        return e;
-    DownArgs d{src, R, b.a, b.as, static_cast<__nv_bfloat16 *>(y), y32, s.E, s.H, s.k, s.I, s.Is, imax, lg,
-               s.k + 1};
-    d.R.idx_out = nullptr;
-    d.R.w_out = nullptr;
-    const size_t ds = down_smem(s, n);
-    return f16 ? down_go<__half>(d, n, ds, st) : down_go<float>(d, n, ds, st);
+        return f16 ? experts_go<1, __half>(A, n, smem, st) : experts_go<1, float>(A, n, smem, st);
+    return f16 ? experts_go<2, __half>(A, n, smem, st) : experts_go<2, float>(A, n, smem, st);
 }
 
 } // namespace tok
