@@ -50,7 +50,11 @@ constexpr int kMaxE = 1024;                          // experts the staged table
 constexpr uint64_t kWaitNs = 200ull * 1000 * 1000;   // 0.2 s bound on any barrier wait
 constexpr int kRec = 80;                             // bytes per fixed-point chunk record
 constexpr int kExThreads = 512;
-constexpr int kMaxChunks = 2;                        // 32-row chunks of a per CTA
+constexpr int kMaxSeg = 2;                           // gate/up segments per CTA
+constexpr int kMaxUnits = 8;                         // gate/up units (8 row pairs) per CTA
+constexpr int kParts = 2;                            // row parts per segment, one barrier each
+constexpr int kRowsPerWarp = 4;                      // gate/up row pairs per warp
+constexpr int kDsPer = 2;                            // down scale pieces per thread
 
 // ------------------------------------------------------------ PTX helpers
 
@@ -131,8 +135,9 @@ __device__ __forceinline__ uint64_t global_ns()
 }
 
 // Wait for phase 0 of a single-use barrier for at most kWaitNs; false (with
-// MOE_ERR_TIMEOUT recorded) if it never completes.
-__device__ __noinline__ bool mbar_wait0(uint64_t *bar)
+// MOE_ERR_TIMEOUT recorded) if it never completes.  Inlined: a call would
+// make the caller's loads still in flight land before it.
+__device__ __forceinline__ bool mbar_wait0(uint64_t *bar)
 {
     if (mbar_try_wait(bar, 0))
         return true;
@@ -184,6 +189,21 @@ __device__ __forceinline__ Chunk load_chunk(const unsigned char *rec)
     c.ho = p[2];
     c.lo = p[3];
     const float2 f = *reinterpret_cast<const float2 *>(rec + 64);
+    c.sx = f.x;
+    c.X = f.y;
+    return c;
+}
+
+// The same from global memory through L2 (written by another CTA).
+__device__ __forceinline__ Chunk load_chunk_global(const unsigned char *rec)
+{
+    Chunk c;
+    const uint4 *p = reinterpret_cast<const uint4 *>(rec);
+    c.he = __ldcg(p);
+    c.le = __ldcg(p + 1);
+    c.ho = __ldcg(p + 2);
+    c.lo = __ldcg(p + 3);
+    const float2 f = __ldcg(reinterpret_cast<const float2 *>(rec + 64));
     c.sx = f.x;
     c.X = f.y;
     return c;
@@ -517,25 +537,26 @@ __global__ void __launch_bounds__(128) router_tok_kernel(const __nv_bfloat16 *__
 // One kernel computes the experts of the token: gate/up SwiGLU, then (after a
 // grid-wide barrier) down + weighted combine.
 //
-// Work: a is cut into 32-row chunks, listed as [shared expert's chunks |
-// rank 0's chunks | rank 1's ...]; CTA c takes chunks c and c + gridDim.x.
-// For a chunk it computes the 32 gate and 32 up rows, a = silu(g) u, and the
-// chunk's fixed-point record, which it writes to global memory in kRep
-// copies.  After the barrier every CTA reads all records and computes output
-// rows [h0, h1) of y from its rows of every active expert's W_d.
+// Gate/up work comes in units of 8 row pairs (gate row o and up row o for 8
+// consecutive o), listed as [shared expert's units | rank 0's units | ...];
+// CTA c takes the contiguous run [c NU / n, (c + 1) NU / n), at most two
+// segments of consecutive rows of one expert.  It computes a = silu(g) u for
+// those rows and writes each unit's part of the fixed-point record of a (see
+// ARec).  After the barrier every CTA computes output rows [h0, h1) of y from
+// its rows of every active expert's W_d, one thread per 32-column chunk of a
+// (and half of the rows).
 //
-// Every weight byte the CTA needs is copied into shared memory right after
-// the routing is known: its chunks' gate and up code rows (bulk copies) and
-// its rows of each active expert's W_d (one bulk copy per expert), plus the
-// scale and bias rows (cp.async by all threads).  Latency-critical reads are
-// kept out of that stream: small reads issued while it is in flight wait
-// behind it.
+// Every code byte the CTA needs is bulk-copied into shared memory right after
+// the routing is known (each segment's gate and up code rows, and its rows of
+// each active expert's W_d), together with plain loads of the scale and bias
+// rows.  Latency-critical reads are kept out of that stream: small reads
+// issued while it is in flight wait behind it.
 struct ExpertsArgs {
     const unsigned char *xrec; // [kRep][xrs] fixed-point records of x
     size_t xrs;
     ExpertSrc src;
     Routing R;
-    unsigned char *arec;       // [kRep][ars]: record of each 32-row chunk of a
+    unsigned char *arec;       // [kRep][ars]: ARec of each 32-row chunk of a
     size_t ars;
     unsigned int *bar;         // grid barrier counter, zeroed by the router kernel
     __nv_bfloat16 *y;
@@ -543,21 +564,27 @@ struct ExpertsArgs {
     int E, k, I, Is, log2G;
 };
 
-// Chunk j of the list: active expert *i (k = shared) and its first row *o0.
-__device__ __forceinline__ void chunk_of(int j, int k, int I, int Is, int *i, int *o0)
+// Fixed-point record of 32 consecutive values of a, written a quarter (8
+// values) at a time: for quarter m, he[m] le[m] ho[m] lo[m] hold the dp4a
+// bytes of its even and odd columns (as in Chunk), sx[m] its step and X[m]
+// its sum.  Quarter m occupies bytes 4m of each 16-byte field.
+constexpr int kArec = 96;
+
+// Active expert *i of gate/up unit u of the list, and its first row *o0.
+__device__ __forceinline__ void unit_of(int u, int k, int I, int Is, int *i, int *o0)
 {
-    const int ns = Is >> 5;
-    if (j < ns) {
+    const int ns = Is >> 3;
+    if (u < ns) {
         *i = k;
-        *o0 = 32 * j;
+        *o0 = 8 * u;
     } else {
-        const int r = (j - ns) / (I >> 5);
+        const int r = (u - ns) / (I >> 3);
         *i = r;
-        *o0 = 32 * ((j - ns) - r * (I >> 5));
+        *o0 = 8 * ((u - ns) - r * (I >> 3));
     }
 }
 
-// Index in the list of chunk ch of active expert i.
+// Index of chunk ch of active expert i in the chunk list [shared | rank 0 | ...].
 __device__ __forceinline__ int chunk_index(int i, int ch, int k, int I, int Is)
 {
     return i == k ? ch : (Is >> 5) + i * (I >> 5) + ch;
@@ -570,18 +597,40 @@ __device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int *p)
     return v;
 }
 
+// s * sum_c q_c a_c + b * sum_c a_c for one 32-code chunk of a W_d row and the
+// ARec fields he..lo (uint4 each, word m = quarter m), sx, X (float4).
+__device__ __forceinline__ float arec_term(uint4 q, uint4 he, uint4 le, uint4 ho, uint4 lo, float4 sx, float4 X,
+                                           float s, float b)
+{
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    const uint32_t H_[4] = {he.x, he.y, he.z, he.w}, L_[4] = {le.x, le.y, le.z, le.w};
+    const uint32_t HO[4] = {ho.x, ho.y, ho.z, ho.w}, LO[4] = {lo.x, lo.y, lo.z, lo.w};
+    const float S[4] = {sx.x, sx.y, sx.z, sx.w};
+    float D = 0.f;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const uint32_t ev = w[m] & 0x0F0F0F0Fu;
+        const uint32_t od = (w[m] >> 4) & 0x0F0F0F0Fu;
+        const int h = dp4a_us(od, HO[m], dp4a_us(ev, H_[m], 0));
+        const int l = dp4a_uu(od, LO[m], dp4a_uu(ev, L_[m], 0));
+        D = fmaf((float)(h * 256 + l), S[m], D);
+    }
+    return fmaf(s, D, b * ((X.x + X.y) + (X.z + X.w)));
+}
+
 // H = 1024 * NXC; TS = scale/bias type.  One CTA of kExThreads per SM.
 //
-// Shared memory (dynamic): per chunk [64 code rows (32 gate, then 32 up)]
-// [64 scale rows][64 bias rows]; then per active expert its down rows (codes
-// [nr][I_i/2], scales and biases [nr][I_i/G] each); then the records of a.
+// Shared memory (dynamic): per segment [n gate code rows][n up code rows]
+// [n gate scale rows][n up scale rows][n gate bias rows][n up bias rows];
+// then per active expert its down rows (codes [nr][I_i/2], scales and biases
+// [nr][I_i/G] each); then the partial sums of the down phase.
 template <int NXC, typename TS>
-__global__ void __launch_bounds__(kExThreads, 1) experts_tok_kernel(ExpertsArgs A)
+__global__ void __maxnreg__(112) experts_tok_kernel(ExpertsArgs A)
 {
     constexpr int H = 1024 * NXC;
     constexpr int NW = kExThreads / 32;
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ uint64_t cbar[kMaxChunks], dbar, xbar;
+    __shared__ uint64_t sbar[kMaxSeg][kParts], dbar, xbar;
     __shared__ int tab[kMaxE];
     __shared__ __align__(16) unsigned char xs[(H / 32) * kRec];
     __shared__ int s_idx[kMaxAct];
@@ -590,7 +639,7 @@ __global__ void __launch_bounds__(kExThreads, 1) experts_tok_kernel(ExpertsArgs 
     __shared__ uint32_t s_eoff[kMaxAct + 1]; // offset of expert i's down rows in the down region
     __shared__ int s_qb[kMaxAct];            // down code bytes per row of expert i
     __shared__ int s_ng[kMaxAct];            // down groups per row of expert i
-    __shared__ __align__(16) float s_a[kMaxChunks][32]; // read as float4
+    __shared__ float s_a[8 * kMaxUnits];
     __shared__ __align__(16) TopkSmem tks;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -598,47 +647,65 @@ __global__ void __launch_bounds__(kExThreads, 1) experts_tok_kernel(ExpertsArgs 
     const int k = A.k, n_act = k + 1;
     const int HG = H >> A.log2G;                     // groups per gate/up row
     const uint32_t qrow = H / 2;                     // code bytes per gate/up row
-    const uint32_t srow = (uint32_t)HG * sizeof(TS); // scale (or bias) bytes per gate/up row
-    const uint32_t cbytes = 64 * (qrow + 2 * srow);  // one chunk in shared memory
     const uint32_t sb = sizeof(TS);
+    const int NU = (A.Is >> 3) + k * (A.I >> 3);
     const int NC = (A.Is >> 5) + k * (A.I >> 5);
-    int nch = 0, cj[kMaxChunks];
-    for (int j = c; j < NC && nch < kMaxChunks; j += n)
-        cj[nch++] = j;
+    const int u0 = (int)((long)c * NU / n), u1 = (int)((long)(c + 1) * NU / n);
+    // segments: runs of this CTA's units within one expert
+    int nseg = 0, seg_i[kMaxSeg], seg_o0[kMaxSeg], seg_n[kMaxSeg];
+    uint32_t seg_off[kMaxSeg];
+    {
+        uint32_t off = 0;
+        for (int u = u0; u < u1 && nseg < kMaxSeg;) {
+            int i, o0;
+            unit_of(u, k, A.I, A.Is, &i, &o0);
+            const int inter = (i == k) ? A.Is : A.I;
+            const int len = min(u1 - u, (inter - o0) >> 3);
+            seg_i[nseg] = i;
+            seg_o0[nseg] = o0;
+            seg_n[nseg] = 8 * len;
+            seg_off[nseg] = off;
+            off += (uint32_t)(8 * len) * (2 * qrow);
+            ++nseg;
+            u += len;
+        }
+    }
+    const int NR = 8 * (u1 - u0); // row pairs of this CTA
+    unsigned char *down = smem + (nseg ? seg_off[nseg - 1] + (uint32_t)seg_n[nseg - 1] * (2 * qrow) : 0u);
     const int h0 = (int)((long)c * (long)H / n), h1 = (int)((long)(c + 1) * (long)H / n);
     const int nr = h1 - h0;
-    unsigned char *down = smem + nch * cbytes;
 
-    // Chunk s: thread `lead` arms its barrier and bulk-copies the 32 gate and
-    // 32 up code rows; every thread cp.asyncs its pieces of the scale and
-    // bias rows and arrives.
-    auto stage_chunk = [&](int s, const char *b, bool lead) {
-        int i, o0;
-        chunk_of(cj[s], k, A.I, A.Is, &i, &o0);
-        const size_t *offs = (i == k) ? A.src.off_sh : A.src.off;
-        unsigned char *d = smem + s * cbytes;
-        if (lead) {
-            mbar_expect_tx(&cbar[s], b ? 64 * qrow : 0u);
-            if (b) {
-                bulk_g2s(d, b + offs[M_QG] + (size_t)o0 * qrow, 32 * qrow, &cbar[s]);
-                bulk_g2s(d + 32 * qrow, b + offs[M_QU] + (size_t)o0 * qrow, 32 * qrow, &cbar[s]);
-            }
+    // The copy warp (the last one; it computes no gate/up rows, since a bulk
+    // copy holds its issuing thread until the copy engine takes it): lane
+    // 2 (s kParts + p) + h copies the gate (h = 0) or up (h = 1) code rows of
+    // part p of segment s (rows [p n / kParts, (p + 1) n / kParts)); the h = 0
+    // lane arms the part's barrier first.  Only segments with `pick` set.
+    auto stage_codes = [&](bool (*pick)(int, int), const char *const *base) {
+        const int q = lane >> 1, h = lane & 1, s = q / kParts, p = q - s * kParts;
+        const bool on = s < nseg && pick(seg_i[s], k) && base[s] != nullptr;
+        uint32_t bytes = 0;
+        int r0 = 0;
+        if (s < nseg) {
+            r0 = p * seg_n[s] / kParts;
+            bytes = (uint32_t)((p + 1) * seg_n[s] / kParts - r0) * qrow;
         }
-        if (b) {
-            unsigned char *ds = d + 64 * qrow;
-            cp_slice(ds, b + offs[M_SG] + (size_t)o0 * srow, 32 * srow, threadIdx.x, kExThreads);
-            cp_slice(ds + 32 * srow, b + offs[M_SU] + (size_t)o0 * srow, 32 * srow, threadIdx.x, kExThreads);
-            cp_slice(ds + 64 * srow, b + offs[M_BG] + (size_t)o0 * srow, 32 * srow, threadIdx.x, kExThreads);
-            cp_slice(ds + 96 * srow, b + offs[M_BU] + (size_t)o0 * srow, 32 * srow, threadIdx.x, kExThreads);
+        if (s < nseg && pick(seg_i[s], k) && h == 0 && bytes)
+            mbar_expect_tx(&sbar[s][p], on ? 2 * bytes : 0u);
+        __syncwarp();
+        if (on && bytes) {
+            const size_t *offs = (seg_i[s] == k) ? A.src.off_sh : A.src.off;
+            const uint32_t nq = (uint32_t)seg_n[s] * qrow;
+            bulk_g2s(smem + seg_off[s] + h * nq + r0 * qrow,
+                     base[s] + offs[h ? M_QU : M_QG] + (size_t)(seg_o0[s] + r0) * qrow, bytes, &sbar[s][p]);
         }
-        cp_arrive(&cbar[s]);
     };
 
     // ---- before the wait: only what does not depend on the router's output
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kMaxChunks; ++s)
-            mbar_init(&cbar[s], kExThreads + 1);
-        mbar_init(&dbar, kExThreads + 1);
+        for (int s = 0; s < kMaxSeg; ++s)
+            for (int p = 0; p < kParts; ++p)
+                mbar_init(&sbar[s][p], 1);
+        mbar_init(&dbar, 1);
         mbar_init(&xbar, kExThreads);
         fence_mbar_init();
         uint32_t o = 0;
@@ -655,10 +722,11 @@ __global__ void __launch_bounds__(kExThreads, 1) experts_tok_kernel(ExpertsArgs 
     for (int e = threadIdx.x; e < A.E; e += kExThreads)
         tab[e] = __ldg(A.src.table + e);
     __syncthreads();
-    // the shared expert's chunks come first in the list: stage them now
-    for (int s = 0; s < nch; ++s)
-        if (cj[s] < (A.Is >> 5))
-            stage_chunk(s, A.src.shared, threadIdx.x == 32 * s);
+    // the shared expert's units come first in the list: stage them now
+    if (warp == NW - 1) {
+        const char *base[kMaxSeg] = {A.src.shared, A.src.shared};
+        stage_codes([](int i, int kk) { return i == kk; }, base);
+    }
 
     // ---- after the wait: x records and the shared-gate logit are fetched
     // while warp 0 selects the top k; then every copy is issued
@@ -673,86 +741,162 @@ __global__ void __launch_bounds__(kExThreads, 1) experts_tok_kernel(ExpertsArgs 
             s_base[lane] = routed_base(A.src, tab, s_idx[lane]);
     }
     __syncthreads();
-    for (int s = 0; s < nch; ++s)
-        if (cj[s] >= (A.Is >> 5)) {
-            int i, o0;
-            chunk_of(cj[s], k, A.I, A.Is, &i, &o0);
-            stage_chunk(s, s_base[i], threadIdx.x == 32 * s);
-        }
-    // down rows: lane i of warp 2 bulk-copies expert i's code rows, lane 0
-    // arms the barrier; every thread stages scale and bias rows
-    if (warp == 2) {
-        const char *b = lane < n_act ? s_base[lane] : nullptr;
-        const uint32_t nq = b ? (uint32_t)nr * s_qb[lane] : 0u;
+    // the copy warp: routed code rows, then expert i's down code rows by lane
+    // 8 + i (lane 8 arms the barrier)
+    if (warp == NW - 1) {
+        const char *base[kMaxSeg];
+        for (int s = 0; s < kMaxSeg; ++s)
+            base[s] = s < nseg ? s_base[seg_i[s]] : nullptr;
+        stage_codes([](int i, int kk) { return i != kk; }, base);
+        const int i = lane - 8;
+        const char *b = (i >= 0 && i < n_act) ? s_base[i] : nullptr;
+        const uint32_t nq = b ? (uint32_t)nr * s_qb[i] : 0u;
         const uint32_t tot = __reduce_add_sync(0xFFFFFFFFu, nq);
-        if (lane == 0)
+        if (lane == 8)
             mbar_expect_tx(&dbar, tot);
         __syncwarp();
         if (b && nq)
-            bulk_g2s(down + s_eoff[lane], b + (lane == k ? A.src.off_sh : A.src.off)[M_QD] + (size_t)h0 * s_qb[lane],
-                     nq, &dbar);
+            bulk_g2s(down + s_eoff[i], b + (i == k ? A.src.off_sh : A.src.off)[M_QD] + (size_t)h0 * s_qb[i], nq,
+                     &dbar);
     }
-    for (int i = 0; i < n_act; ++i) {
-        const char *b = s_base[i];
-        if (!b)
-            continue;
-        const size_t *offs = (i == k) ? A.src.off_sh : A.src.off;
-        const uint32_t nq = (uint32_t)nr * s_qb[i], ns = (uint32_t)nr * s_ng[i] * sb;
-        unsigned char *d = down + s_eoff[i];
-        cp_slice(d + nq, b + offs[M_SD] + (size_t)h0 * s_ng[i] * sb, ns, threadIdx.x, kExThreads);
-        cp_slice(d + nq + ns, b + offs[M_BD] + (size_t)h0 * s_ng[i] * sb, ns, threadIdx.x, kExThreads);
+    // scale and bias values by plain loads, issued with the copies: each
+    // lane's group of its warp's gate/up rows (in registers), and this CTA's
+    // rows of every expert's down scales and biases (stored before the grid
+    // barrier)
+    constexpr int NWC = NW - 1; // gate/up warps
+    float gsc[kRowsPerWarp][4]; // gate scale, gate bias, up scale, up bias
+#pragma unroll
+    for (int t = 0; t < kRowsPerWarp; ++t) {
+        const int rp = warp < NWC ? warp + t * NWC : NR;
+        gsc[t][0] = gsc[t][1] = gsc[t][2] = gsc[t][3] = 0.f;
+        if (rp < NR) {
+            const int s = (nseg > 1 && rp >= seg_n[0]) ? 1 : 0, r = s ? rp - seg_n[0] : rp;
+            const char *b = s_base[seg_i[s]];
+            if (b) {
+                const size_t *offs = (seg_i[s] == k) ? A.src.off_sh : A.src.off;
+                const size_t ro = (size_t)(seg_o0[s] + r) * HG + (NXC * lane * 32 >> A.log2G);
+                gsc[t][0] = ld_sb(reinterpret_cast<const TS *>(b + offs[M_SG]) + ro);
+                gsc[t][1] = ld_sb(reinterpret_cast<const TS *>(b + offs[M_BG]) + ro);
+                gsc[t][2] = ld_sb(reinterpret_cast<const TS *>(b + offs[M_SU]) + ro);
+                gsc[t][3] = ld_sb(reinterpret_cast<const TS *>(b + offs[M_BU]) + ro);
+            }
+        }
     }
-    cp_arrive(&dbar);
+    // down scale/bias pieces: routed expert i owns pieces [i pr, (i+1) pr),
+    // the shared expert the next ps; the first half of an expert's pieces
+    // are scale rows, the second half bias rows
+    const int pr = 2 * nr * s_ng[0] * (int)sb / 16, ps = 2 * nr * s_ng[k] * (int)sb / 16;
+    uint4 dv[kDsPer];
+    int dp[kDsPer];
+#pragma unroll
+    for (int u = 0; u < kDsPer; ++u) {
+        const int P = threadIdx.x + u * kExThreads;
+        const int i = P < k * pr ? P / pr : k, q = P < k * pr ? P - i * pr : P - k * pr, np = i < k ? pr : ps;
+        dp[u] = -1;
+        if (q < np && s_base[i]) {
+            const size_t *offs = (i == k) ? A.src.off_sh : A.src.off;
+            const int a = q >= np / 2, off = (q - a * (np / 2)) * 16;
+            dv[u] = __ldg(reinterpret_cast<const uint4 *>(s_base[i] + offs[a ? M_BD : M_SD] +
+                                                          (size_t)h0 * s_ng[i] * sb + off));
+            dp[u] = (int)s_eoff[i] + nr * s_qb[i] + a * nr * s_ng[i] * (int)sb + off;
+        }
+    }
 
-    // ---- gate/up: warp w computes row pairs w and w + 16 of each chunk
+    // ---- gate/up: warp w < NWC computes row pairs w, w + NWC, ...
     if (!__all_sync(0xFFFFFFFFu, mbar_wait0(&xbar)))
         return;
     Chunk xv[NXC];
-    int grp[NXC];
 #pragma unroll
-    for (int m = 0; m < NXC; ++m) {
+    for (int m = 0; m < NXC; ++m)
         xv[m] = load_chunk(xs + (size_t)(NXC * lane + m) * kRec);
-        grp[m] = ((NXC * lane + m) * 32) >> A.log2G;
-    }
-    for (int s = 0; s < nch; ++s) {
-        int i, o0;
-        chunk_of(cj[s], k, A.I, A.Is, &i, &o0);
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait0(&cbar[s])))
-            return;
-        const unsigned char *d = smem + s * cbytes;
-        const TS *sc = reinterpret_cast<const TS *>(d + 64 * qrow);
-        const TS *bi = sc + 64 * HG;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f}; // gate t0, up t0, gate t1, up t1
-        if (s_base[i]) {
+    uint32_t waited = 0; // bit s kParts + p: part p of segment s has landed
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                const int row = (v & 1) * 32 + warp + (v >> 1) * NW; // smem row of this gate/up row
-                const uint4 *q = reinterpret_cast<const uint4 *>(d + (size_t)row * qrow);
+    for (int t = 0; t < kRowsPerWarp; ++t) {
+        const int rp = warp < NWC ? warp + t * NWC : NR;
+        if (rp >= NR)
+            break;
+        const int s = (nseg > 1 && rp >= seg_n[0]) ? 1 : 0, r = s ? rp - seg_n[0] : rp;
+        const int p = ((r + 1) * kParts - 1) / seg_n[s]; // part of row r
+        const uint32_t bit = 1u << (s * kParts + p);
+        if (!(waited & bit)) {
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait0(&sbar[s][p])))
+                return;
+            waited |= bit;
+        }
+        float g = 0.f, u = 0.f;
+        if (s_base[seg_i[s]]) {
+            const uint32_t nq = (uint32_t)seg_n[s] * qrow;
+            const unsigned char *d = smem + seg_off[s];
+            const uint4 *qg = reinterpret_cast<const uint4 *>(d + (size_t)r * qrow);
+            const uint4 *qu = reinterpret_cast<const uint4 *>(d + nq + (size_t)r * qrow);
+            int dg[NXC], du[NXC];
 #pragma unroll
-                for (int m = 0; m < NXC; ++m)
-                    acc[v] += chunk_term(q[NXC * lane + m], xv[m], ld_sb(sc + row * HG + grp[m]),
-                                         ld_sb(bi + row * HG + grp[m]));
+            for (int m = 0; m < NXC; ++m) {
+                dg[m] = chunk_idot(qg[NXC * lane + m], xv[m]);
+                du[m] = chunk_idot(qu[NXC * lane + m], xv[m]);
             }
+            // one quantisation group per lane: sum_m s (sx_m D_m) + b X_m
+            float Dg = 0.f, Du = 0.f, Xs = 0.f;
+#pragma unroll
+            for (int m = 0; m < NXC; ++m) {
+                Dg = fmaf((float)dg[m], xv[m].sx, Dg);
+                Du = fmaf((float)du[m], xv[m].sx, Du);
+                Xs += xv[m].X;
+            }
+            g = fmaf(gsc[t][0], Dg, gsc[t][1] * Xs);
+            u = fmaf(gsc[t][2], Du, gsc[t][3] * Xs);
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-                acc[v] += __shfl_xor_sync(0xFFFFFFFFu, acc[v], o);
-        if (lane == 0) {
-            s_a[s][warp] = acc[0] * sigmoid_f(acc[0]) * acc[1];
-            s_a[s][warp + NW] = acc[2] * sigmoid_f(acc[2]) * acc[3];
+        for (int o = 16; o > 0; o >>= 1) {
+            g += __shfl_xor_sync(0xFFFFFFFFu, g, o);
+            u += __shfl_xor_sync(0xFFFFFFFFu, u, o);
         }
+        if (lane == 0)
+            s_a[rp] = g * sigmoid_f(g) * u;
     }
+#pragma unroll
+    for (int uu = 0; uu < kDsPer; ++uu)
+        if (dp[uu] >= 0)
+            *reinterpret_cast<uint4 *>(down + dp[uu]) = dv[uu];
     __syncthreads();
-    // chunk records: warp s, lanes 0..7, four values each
-    if (warp < nch) {
-        const float4 v = *reinterpret_cast<const float4 *>(&s_a[warp][4 * (lane & 7)]);
-        const float f[4] = {v.x, v.y, v.z, v.w};
-        store_chunk4(f, A.arec + (size_t)cj[warp] * kRec, lane, lane < 8, kRep, A.ars);
+    // each unit writes its quarter of a chunk's record, in kRep copies
+    if (threadIdx.x < u1 - u0) {
+        const int uu = u0 + threadIdx.x;
+        int i, o0;
+        unit_of(uu, k, A.I, A.Is, &i, &o0);
+        const float *v = s_a + 8 * threadIdx.x;
+        float am = 0.f, X = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            am = fmaxf(am, fabsf(v[j]));
+            X += v[j];
+        }
+        const bool nz = am > 0.f && am < INFINITY;
+        const float inv = nz ? 32767.0f / am : 0.f;
+        uint32_t f[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            f[j] = __float_as_uint(fmaf(v[j], inv, 12582912.0f));
+        // byte j of he / le: columns 2j (high / low byte); of ho / lo: 2j + 1
+        const uint32_t e01 = __byte_perm(f[0], f[2], 0x5140), e23 = __byte_perm(f[4], f[6], 0x5140);
+        const uint32_t o01 = __byte_perm(f[1], f[3], 0x5140), o23 = __byte_perm(f[5], f[7], 0x5140);
+        const uint32_t he = __byte_perm(e01, e23, 0x7632), le = __byte_perm(e01, e23, 0x5410);
+        const uint32_t ho = __byte_perm(o01, o23, 0x7632), lo = __byte_perm(o01, o23, 0x5410);
+        const int m = (o0 & 31) >> 3;
+        unsigned char *rec = A.arec + (size_t)chunk_index(i, o0 >> 5, k, A.I, A.Is) * kArec + 4 * m;
+        const float sx = nz ? am / 32767.0f : 0.f;
+        for (int r = 0; r < kRep; ++r) {
+            unsigned char *rr = rec + (size_t)r * A.ars;
+            *reinterpret_cast<uint32_t *>(rr) = he;
+            *reinterpret_cast<uint32_t *>(rr + 16) = le;
+            *reinterpret_cast<uint32_t *>(rr + 32) = ho;
+            *reinterpret_cast<uint32_t *>(rr + 48) = lo;
+            *reinterpret_cast<float *>(rr + 64) = sx;
+            *reinterpret_cast<float *>(rr + 80) = X;
+        }
     }
 
-    // ---- grid barrier: every chunk record is written
+    // ---- grid barrier: every record is written
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
@@ -767,63 +911,69 @@ __global__ void __launch_bounds__(kExThreads, 1) experts_tok_kernel(ExpertsArgs 
     }
     __syncthreads();
     pdl_trigger(); // the next layer call may start its own weight loads now
-    unsigned char *arec = down + ((s_eoff[n_act] + 15) & ~15u);
-    {
-        const uint4 *src = reinterpret_cast<const uint4 *>(A.arec + (size_t)rep * A.ars);
-        uint4 *dst = reinterpret_cast<uint4 *>(arec);
-        for (int q = threadIdx.x; q < NC * kRec / 16; q += kExThreads)
-            dst[q] = __ldcg(src + q);
-    }
-    __syncthreads();
-    const bool ready = __all_sync(0xFFFFFFFFu, mbar_wait0(&dbar));
 
-    // ---- down: warp w computes output row w; lane l & 15 takes chunks l,
-    // l+16, ... of the row for the experts of parity l >> 4 (rank order,
-    // shared last), two experts at a time; the warp sums its lanes in a
-    // fixed tree, so the order does not depend on where the experts live
-    const int par = lane >> 4, l16 = lane & 15;
-    const int hr = warp;
-    float acc = 0.f;
-    if (ready && hr < nr) {
-        constexpr int U = 2;
-#pragma unroll 1
-        for (int i0 = 0; i0 < n_act; i0 += 2 * U) {
-            for (int ch0 = 0;; ch0 += 16) {
-                uint4 q[U];
-                Chunk av[U];
-                float sc[U], bc[U], wi[U];
-                bool any = false;
+    // ---- down, item by item: thread t < 2 NC owns chunk j = t % NC (chunk ch
+    // of active expert i; its record is loaded into registers) and half the
+    // CTA's output rows, [rg RH, rg RH + RH) with rg = t / NC.  It writes w_i
+    // times its part of each row to P[row][j]; warp w then sums row w over
+    // the chunks in a fixed order, so the result does not depend on where the
+    // experts live.
+    const int RH = (nr + 1) / 2;
+    float *P = reinterpret_cast<float *>(down + ((s_eoff[n_act] + 15) & ~15u)); // [nr][NC]
+    const int t = threadIdx.x;
+    const bool mine = t < 2 * NC;
+    const int j = mine ? t % NC : 0, rg = t / NC;
+    int ii, ch;
+    if (j < (A.Is >> 5)) {
+        ii = k;
+        ch = j;
+    } else {
+        ii = (j - (A.Is >> 5)) / (A.I >> 5);
+        ch = (j - (A.Is >> 5)) - ii * (A.I >> 5);
+    }
+    uint4 rv[6] = {};
+    if (mine) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(A.arec + (size_t)rep * A.ars + (size_t)j * kArec);
 #pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int i = i0 + 2 * u + par;
-                    const int ic = min(i, n_act - 1);
-                    const int qb = s_qb[ic], ng = s_ng[ic];
-                    const int ch = ch0 + l16;
-                    const bool live = i < n_act && s_base[ic] != nullptr && ch < (qb >> 4);
-                    any |= ch0 < (qb >> 4) && i < n_act;
-                    const int chc = live ? ch : 0;
-                    const unsigned char *d = down + s_eoff[ic];
-                    const TS *sd = reinterpret_cast<const TS *>(d + nr * qb) + hr * ng;
-                    const int g = (chc * 32) >> A.log2G;
-                    q[u] = reinterpret_cast<const uint4 *>(d + hr * qb)[chc];
-                    av[u] = load_chunk(arec + (size_t)chunk_index(ic, chc, k, A.I, A.Is) * kRec);
-                    sc[u] = ld_sb(sd + g);
-                    bc[u] = ld_sb(sd + nr * ng + g);
-                    wi[u] = live ? ((i < k) ? s_w[i] : s_w[kMaxAct]) : 0.f;
-                }
-                if (!__any_sync(0xFFFFFFFFu, any))
-                    break;
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-                    acc = fmaf(wi[u], chunk_term(q[u], av[u], sc[u], bc[u]), acc);
+        for (int q = 0; q < 6; ++q)
+            rv[q] = __ldcg(src + q);
+    }
+    const bool ready = __all_sync(0xFFFFFFFFu, mbar_wait0(&dbar));
+    if (mine) {
+        const int r0 = rg * RH, r1 = min(nr, r0 + RH);
+        if (ready && s_base[ii]) {
+            const int qb = s_qb[ii], ng = s_ng[ii];
+            const unsigned char *d = down + s_eoff[ii];
+            const TS *sd = reinterpret_cast<const TS *>(d + nr * qb);
+            const TS *bd = sd + nr * ng;
+            const int g = (ch * 32) >> A.log2G;
+            const float wi = ii < k ? s_w[ii] : s_w[kMaxAct];
+            const float4 sx = make_float4(__uint_as_float(rv[4].x), __uint_as_float(rv[4].y),
+                                          __uint_as_float(rv[4].z), __uint_as_float(rv[4].w));
+            const float4 X = make_float4(__uint_as_float(rv[5].x), __uint_as_float(rv[5].y),
+                                         __uint_as_float(rv[5].z), __uint_as_float(rv[5].w));
+#pragma unroll 4
+            for (int r = r0; r < r1; ++r) {
+                const uint4 q = reinterpret_cast<const uint4 *>(d + r * qb)[ch];
+                P[r * NC + j] = wi * arec_term(q, rv[0], rv[1], rv[2], rv[3], sx, X, ld_sb(sd + r * ng + g),
+                                               ld_sb(bd + r * ng + g));
             }
+        } else {
+            for (int r = r0; r < r1; ++r)
+                P[r * NC + j] = 0.f;
         }
     }
-    acc = warp_sum(acc);
-    if (ready && hr < nr && lane == 0) {
-        A.y[h0 + hr] = __float2bfloat16_rn(acc);
-        if (A.y32)
-            A.y32[h0 + hr] = acc;
+    __syncthreads();
+    for (int r = warp; r < nr; r += NW) {
+        float acc = 0.f;
+        for (int q = lane; q < NC; q += 32)
+            acc += P[r * NC + q];
+        acc = warp_sum(acc);
+        if (ready && lane == 0) {
+            A.y[h0 + r] = __float2bfloat16_rn(acc);
+            if (A.y32)
+                A.y32[h0 + r] = acc;
+        }
     }
 }
 
@@ -868,11 +1018,16 @@ static int log2i(int v)
     return l;
 }
 
-// Dynamic shared memory of the experts kernel for a CTA with `nch` chunks.
-static size_t experts_smem(const Shape &s, int n, int nch)
+// Gate/up units (8 row pairs) and 32-row chunks of a of one token.
+static int n_units(const Shape &s) { return s.Is / 8 + s.k * (s.I / 8); }
+static int n_chunks(const Shape &s) { return s.Is / 32 + s.k * (s.I / 32); }
+
+// Dynamic shared memory of the experts kernel (the largest CTA share).
+static size_t experts_smem(const Shape &s, int n)
 {
     const size_t sb = s.qscale == MOE_F16 ? 2 : 4;
-    const size_t chunk = 64 * ((size_t)s.H / 2 + 2 * (size_t)(s.H / s.G) * sb);
+    const size_t rowpair = (size_t)s.H; // gate and up code rows
+    const int units = (n_units(s) + n - 1) / n;
     const int nr = (s.H + n - 1) / n;
     size_t w = 0;
     for (int i = 0; i <= s.k; ++i) {
@@ -880,14 +1035,7 @@ static size_t experts_smem(const Shape &s, int n, int nch)
         w += (size_t)nr * (inter / 2 + 2 * (inter / s.G) * sb);
     }
     w = (w + 15) & ~(size_t)15;
-    const int NC = s.Is / 32 + s.k * (s.I / 32);
-    return nch * chunk + w + (size_t)kRec * NC;
-}
-
-static int max_chunks(const Shape &s, int n)
-{
-    const int NC = s.Is / 32 + s.k * (s.I / 32);
-    return (NC + n - 1) / n;
+    return 8 * (size_t)units * rowpair + w + sizeof(float) * (size_t)nr * n_chunks(s);
 }
 
 constexpr size_t kSmemLimit = 220 * 1024;
@@ -905,14 +1053,24 @@ bool eligible(const Shape &s)
     const int sb = s.qscale == MOE_F16 ? 2 : 4;
     if (((s.H / s.G) * sb) % 16 || ((s.I / s.G) * sb) % 16 || ((s.Is / s.G) * sb) % 16)
         return false;
-    if (s.I % 32 || s.Is % 32 || s.G < 32)
+    if (s.I % 32 || s.Is % 32 || s.G < 64) // one quantisation group per lane of a gate/up row
         return false;
     const int n = sm_count();
-    if (max_chunks(s, n) > kMaxChunks)        // a CTA owns at most kMaxChunks chunks of a
+    const int units = (n_units(s) + n - 1) / n;
+    if (units > kMaxUnits || 8 * units > s.I || 8 * units > s.Is) // at most two segments per CTA
         return false;
-    if ((s.H + n - 1) / n > kExThreads / 32)  // down: one output row per warp
+    if (2 * n_chunks(s) > kExThreads) // down: one thread per (chunk, half of the rows)
         return false;
-    return experts_smem(s, n, max_chunks(s, n)) <= kSmemLimit;
+    const int nr = (s.H + n - 1) / n;
+    if (nr > 2 * (kExThreads / 32)) // down: output rows per CTA
+        return false;
+    if (8 * units > kRowsPerWarp * (kExThreads / 32 - 1)) // gate/up row pairs per warp
+        return false;
+    if (8 + s.k + 1 > 32 || 2 * kMaxSeg * kParts > 8) // lanes of the copy warp
+        return false;
+    if (2 * nr * ((s.k * (s.I / s.G) + s.Is / s.G) * sb) / 16 > kDsPer * kExThreads) // down scale pieces
+        return false;
+    return experts_smem(s, n) <= kSmemLimit;
 }
 
 // All three kernels run with the same (maximal) shared-memory carveout: an SM
@@ -933,19 +1091,17 @@ static size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 size_t bufs_bytes(const Shape &s)
 {
-    const int NC = s.Is / 32 + s.k * (s.I / 32);
     const size_t lg = up256(sizeof(float) * (size_t)(s.E + 1));
     const size_t xr = up256((size_t)kRec * (s.H / 32));
-    const size_t ar = up256((size_t)kRec * NC);
+    const size_t ar = up256((size_t)kArec * n_chunks(s));
     return kRep * (lg + xr + ar) + 256;
 }
 
 Bufs bufs_carve(const Shape &s, char *base)
 {
-    const int NC = s.Is / 32 + s.k * (s.I / 32);
     const size_t lg = up256(sizeof(float) * (size_t)(s.E + 1));
     const size_t xr = up256((size_t)kRec * (s.H / 32));
-    const size_t ar = up256((size_t)kRec * NC);
+    const size_t ar = up256((size_t)kArec * n_chunks(s));
     Bufs b;
     b.lg = reinterpret_cast<float *>(base);
     b.lgs = (int)(lg / sizeof(float));
@@ -1002,7 +1158,7 @@ cudaError_t launch_experts(const Shape &s, const Bufs &b, const ExpertSrc &src, 
     const int n = sm_count();
     ExpertsArgs A{b.xrec, b.xrs, src, R, b.arec, b.ars, b.bar, static_cast<__nv_bfloat16 *>(y), y32,
                   s.E, s.k, s.I, s.Is, log2i(s.G)};
-    const size_t smem = experts_smem(s, n, max_chunks(s, n));
+    const size_t smem = experts_smem(s, n);
     const bool f16 = s.qscale == MOE_F16;
     if (s.H == 1024)
         return f16 ? experts_go<1, __half>(A, n, smem, st) : experts_go<1, float>(A, n, smem, st);
