@@ -13,19 +13,32 @@ weights from being served by the 126 MB L2, consecutive tokens rotate through
 R full copies of the layer (R chosen so the rotating working set is at least
 3x L2).
 
-Reported: tokens/s (whole job, all ranks), the layer step's achieved HBM
+Reported: tokens/s (whole job, all ranks), the layer call's achieved HBM
 bandwidth on algorithmic bytes (active expert bytes over the event-timed
-duration of sampled layer calls) against the measured copy peak, the oracle's
+mean duration of one layer call) against the measured copy peak, the oracle's
 CPU throughput on a bounded sample, and an end-to-end number through the
 public C-ABI calls with pinned host buffers and copies inside the timed
 region.  Multi-GPU runs are independent replicas (the layer does not shard
 at batch 1); no collective touches the data path.
 
 `--impl reference` times the CPU oracle instead (rank 0 only).
+
+Two more workloads print their own line (not the default):
+
+- `--workload 80b-prefill`: one step = one 4096-token layer call (Zipf-skewed
+  routing, tcgen05 grouped GEMMs); tokens/s and TFLOP/s on algorithmic flops
+  against the measured bf16 peak.
+- `--workload 80b-stack`: one step = one decode token through a 48-layer
+  stack served from a bounded HBM slot pool (25% of each layer's experts,
+  LFU+recency, misses filled from pinned host memory on a side stream);
+  tokens/s, hit rate, misses and exposed copy time per token, the measured
+  pinned host-to-device copy rate, and bit-identity of every layer output
+  with an all-resident run of the same stack.
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -45,7 +58,7 @@ from int4_routed_expert_06_b300 import synth  # noqa: E402
 METRIC = "routed-MoE layer tokens/s (decode, 512e top-10 int4); HBM GB/s vs peak"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6400.0
-KERNELS_PER_TOKEN = 3  # single-token path: router, gate/up SwiGLU (+ top-k), down + combine (+ top-k)
+KERNELS_PER_TOKEN = 2  # single-token path: router (+ x records), experts (top-k, gate/up SwiGLU, down + combine)
 
 
 def peaks():
@@ -56,6 +69,24 @@ def peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per layer call from the committed ncu capture, or None when
+    the single-token kernel source has changed since the counters were taken."""
+    src = os.path.join(ROOT, "int4_routed_expert_06_b300", "csrc", "kernels_token.cu")
+    rec = os.path.join(ROOT, "profiles", "decode_layer_traffic.txt")
+    try:
+        with open(src, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+        with open(rec) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) == 5 and not line.startswith("#") and parts[0] == workload:
+                    return int(parts[4]) if parts[1] == digest else None
+    except OSError:
+        return None
+    return None
 
 
 def workload_desc(shape) -> str:
@@ -76,10 +107,14 @@ class ClockSampler:
         self.proc = None
 
     def __enter__(self):
+        # The timed region starts only once nvidia-smi has printed its first
+        # sample: its start-up work in the driver otherwise lands inside it.
+        self.first = ""
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.first = self.proc.stdout.readline()
         except Exception:
             self.proc = None
         return self
@@ -89,7 +124,8 @@ class ClockSampler:
         if self.proc is not None:
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                rest, _ = self.proc.communicate(timeout=5)
+                self.out = rest  # the first sample was taken before the timed region
             except Exception:
                 self.proc.kill()
 
@@ -134,7 +170,11 @@ def run_reference(args, shape, rank):
         return
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     w = synth.make_layer(shape, device=dev)
-    xs = synth.decode_xs(shape, max(args.steps + args.warmup, 1), device=dev)
+    n = max(args.steps + args.warmup, 1)
+    if shape.name == "80b-prefill":  # tokens of the seeded 4096-token batch, one at a time
+        xs = synth.make_x(shape, synth.PREFILL_X_SEED, device=dev)[:n]
+    else:
+        xs = synth.decode_xs(shape, n, device=dev)
     from oracle import oracle as O
     L = O.Layer(w, shape.group, shape.top_k)
     for j in range(args.warmup):
@@ -143,7 +183,9 @@ def run_reference(args, shape, rank):
     for j in range(args.steps):
         L.forward(xs[args.warmup + j:args.warmup + j + 1])
     dt = time.perf_counter() - t0
-    v = args.steps / dt
+    # a stack token is one pass through every layer: the oracle's per-layer
+    # rate divided by the layer count (layer 0's weights stand for all)
+    v = args.steps / dt / max(shape.layers, 1)
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / max(args.steps, 1) * 1e3,
@@ -156,6 +198,242 @@ def run_reference(args, shape, rank):
     }), flush=True)
 
 
+# ---------------------------------------------------------------- prefill
+
+def prefill_flops(shape, T: int) -> int:
+    """Algorithmic flops of one T-token layer call: router (E rows + shared
+    gate), k routed and one shared SwiGLU expert per token (gate, up, down)."""
+    H = shape.hidden
+    per_tok = (2 * H * (shape.n_experts + 1) + shape.top_k * 6 * H * shape.inter
+               + (6 * H * shape.shared_inter if shape.shared_inter else 0))
+    return T * per_tok
+
+
+def run_prefill(args, shape):
+    from int4_routed_expert_06_b300 import binding as B
+    from int4_routed_expert_06_b300 import build as _build
+    _build.build()
+    torch.cuda.set_device(0)
+    T = shape.tokens
+    w = synth.make_layer(shape, device="cuda")
+    dl = B.DeviceLayer(shape, w, synth.shuffled_slots(shape.n_experts, shape.weight_seed))
+    x = synth.make_x(shape, synth.PREFILL_X_SEED, device="cuda")
+    y = torch.empty((T, shape.hidden), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((T, shape.top_k), dtype=torch.int32, device="cuda")
+    cfg = dl.cfg
+    nb = B.moe_layer_workspace_bytes(cfg, T)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()  # inputs were made on the default stream
+
+    def step():
+        B.moe_layer_forward(cfg, dl.struct(), x, T, y, None, idx, None, ws, nb, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert B.moe_get_device_error(stream) == 0
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("prefill_steps")  # lets a profiler select the timed launches
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        end.record(stream)
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / args.steps
+    if B.moe_get_device_error(stream) != 0:
+        raise RuntimeError("a kernel recorded a device error during the bench")
+    counts = torch.bincount(idx.flatten().long(), minlength=shape.n_experts)
+    flops = prefill_flops(shape, T)
+    tf = flops / (ms * 1e-3) / 1e12
+    pk = peak_bf16()
+    # end to end: pinned x in, pinned y out, around the same call
+    xh, yh = x.cpu().pin_memory(), torch.empty_like(y, device="cpu").pin_memory()
+    xd = torch.empty_like(x)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_e2e = min(args.steps, 5)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n_e2e):
+            xd.copy_(xh, non_blocking=True)
+            B.moe_layer_forward(cfg, dl.struct(), xd, T, y, None, idx, None, ws, nb, stream)
+            yh.copy_(y, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e = n_e2e * T / (e0.elapsed_time(e1) * 1e-3)
+    print(json.dumps({
+        "metric": "routed-MoE layer prefill tokens/s (4096 tokens, 512e top-10 int4, Zipf-skewed routing)",
+        "value": T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 MMA (f32 accumulate in TMEM)", "data": "synthetic",
+        "config": {"workload": f"80b-prefill: T={T}, H={shape.hidden} E={shape.n_experts} top-{shape.top_k} "
+                               f"I={shape.inter} shared I={shape.shared_inter}, int4 g{shape.group} f16 "
+                               f"scale/bias, Zipf(s={shape.zipf_s}) router bias",
+                   "l2": "inputs larger than L2: every step reads all 512 experts' weights (906 MB)",
+                   "experts_used": int((counts > 0).sum()), "max_tokens_per_expert": int(counts.max()),
+                   "min_tokens_per_used_expert": int(counts[counts > 0].min())},
+        "roofline": {"kernel": "prefill layer call (router, top-k, bucketing, gather, tcgen05 grouped GEMMs "
+                               "gate/up and down, combine), timed as one unit",
+                     "bound": "tensor", "achieved": tf, "peak": pk[0], "peak_kind": pk[1], "unit": "TFLOP/s",
+                     "frac": tf / pk[0], "traffic": None, "algorithmic_flops_per_launch": flops},
+        "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": xh.numel() * 2,
+                "d2h_bytes_per_step": yh.numel() * 2},
+        "clocks": clk.summary(),
+    }), flush=True)
+
+
+def peak_bf16():
+    """Sustained dense bf16 TFLOP/s (a step timed inside a long loop)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops_sustained"]), "measured, sustained"
+    except Exception:
+        return 1400.0, "fallback, sustained"
+
+
+# ---------------------------------------------------------------- stack
+
+def host_bytes_available() -> int:
+    avail = 0
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    avail = int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    try:
+        with open("/sys/fs/cgroup/memory.max") as f:
+            v = f.read().strip()
+        if v != "max":
+            with open("/sys/fs/cgroup/memory.current") as f:
+                cur = int(f.read().strip())
+            avail = min(avail, int(v) - cur)
+    except (OSError, ValueError):
+        pass
+    return avail
+
+
+def run_stack(args, shape):
+    from int4_routed_expert_06_b300 import binding as B
+    from int4_routed_expert_06_b300 import build as _build
+    from int4_routed_expert_06_b300.stack import PooledStack, layer_input
+    _build.build()
+    torch.cuda.set_device(0)
+    E, k = shape.n_experts, shape.top_k
+    per_layer = E * synth.expert_bytes(shape)
+    L = shape.layers
+    fit = int(0.6 * host_bytes_available()) // per_layer
+    if fit < L:
+        L = max(1, fit)
+    resident = []
+
+    def weights(l):
+        w = synth.make_layer(shape, seed=shape.weight_seed + l, device="cuda")
+        resident.append(B.DeviceLayer(shape, w, torch.arange(E, dtype=torch.int32)))
+        return w
+
+    t_build = time.perf_counter()
+    st = PooledStack(shape, L, shape.pool_slots, weights)
+    t_build = time.perf_counter() - t_build
+    n = args.warmup + args.steps
+    x0 = synth.decode_xs(shape, n, seed0=synth.STACK_X_SEED0, device="cuda")
+    Y = torch.empty((n, L, shape.hidden), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def token(j):
+        h = x0[j:j + 1]
+        for l in range(L):
+            st.layer_forward(l, layer_input(h), Y[j, l:l + 1])
+            h = (h.float() + Y[j, l:l + 1].float()).to(torch.bfloat16)
+
+    for j in range(args.warmup):
+        token(j)
+    torch.cuda.synchronize()
+    s0 = st.stats()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        t_wall = time.perf_counter()
+        start.record(stream)
+        for j in range(args.warmup, n):
+            token(j)
+        end.record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    ms = start.elapsed_time(end)
+    s1 = st.stats()
+    if B.moe_get_device_error() != 0:
+        raise RuntimeError("a kernel recorded a device error during the bench")
+    d = {key: s1[key] - s0[key] for key in ("hits", "misses", "evictions", "bytes_filled", "exposed_copy_ns",
+                                             "lookups")}
+    # the same tokens through all-resident layers: timing, and bit-identity of every layer output
+    cfg = st.cfg
+    nb = B.moe_layer_workspace_bytes(cfg, 1)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    yr = torch.empty((1, shape.hidden), dtype=torch.bfloat16, device="cuda")
+    mism = torch.zeros((), dtype=torch.int64, device="cuda")
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    r0.record(stream)
+    for j in range(args.warmup, n):
+        h = x0[j:j + 1]
+        for l in range(L):
+            B.moe_layer_forward(cfg, resident[l].struct(), layer_input(h), 1, yr, None, None, None, ws, nb)
+            mism += (yr != Y[j, l:l + 1]).any()
+            h = (h.float() + yr.float()).to(torch.bfloat16)
+    r1.record(stream)
+    torch.cuda.synchronize()
+    res_ms = r0.elapsed_time(r1)
+    n_mism = int(mism.item())
+    # pinned host -> device copy rate for blob-sized copies (the fills' own size)
+    blob = st.blob_bytes
+    dst = torch.empty((64, blob), dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(side):
+        for rep in range(2):
+            c0.record(side)
+            for i in range(64):
+                dst[i].copy_(st.backing[0, i, :blob], non_blocking=True)
+            c1.record(side)
+    torch.cuda.synchronize()
+    h2d_gbs = 64 * blob / (c0.elapsed_time(c1) * 1e-3) / 1e9
+    K = args.steps
+    lookups = max(d["hits"] + d["misses"], 1)
+    print(json.dumps({
+        "metric": "80B-stack decode tokens/s through a bounded HBM expert pool (25% of experts per layer)",
+        "value": K / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "s32/f32", "data": "synthetic",
+        "config": {"workload": f"80b-stack: {L} layers (of {shape.layers}) x E={E} top-{k}, "
+                               f"{shape.pool_slots} slots/layer, Zipf(s={shape.zipf_s}) router bias, "
+                               "residual stream h_(l+1) = bf16(h_l + y_l), layer input bf16(h_l / rms(h_l)), batch-1 decode",
+                   "layers_run": L, "layers_named": shape.layers,
+                   "host_memory_note": (None if L == shape.layers else
+                                        f"pinned backing store limited to {L} layers by host memory"),
+                   "l2": f"pool {L * shape.pool_slots * st.stride / 1e9:.1f} GB and {L} resident layers, "
+                         "far beyond L2", "build_s": t_build},
+        "pool": {"hit_rate": d["hits"] / lookups, "misses_per_token": d["misses"] / K,
+                 "fill_bytes_per_token": d["bytes_filled"] / K, "evictions": d["evictions"],
+                 "exposed_copy_us_per_token": d["exposed_copy_ns"] / 1e3 / K,
+                 "pcie_h2d_gbs_blob_copies": h2d_gbs,
+                 "copy_bound_us_per_token": d["bytes_filled"] / K / (h2d_gbs * 1e9) * 1e6},
+        "resident": {"tokens_per_s": K / (res_ms * 1e-3), "note": "same tokens, all experts resident, eager calls"},
+        "bit_identical_to_resident": n_mism == 0, "mismatched_layer_outputs": n_mism,
+        "all_outputs_finite": bool(torch.isfinite(Y[args.warmup:].float()).all()),
+        "layer_outputs_compared": K * L,
+        "roofline": {"bound": "pcie", "achieved": d["bytes_filled"] / (ms * 1e-3) / 1e9,
+                     "peak": h2d_gbs, "unit": "GB/s", "frac": d["bytes_filled"] / (ms * 1e-3) / 1e9 / h2d_gbs,
+                     "traffic": None, "peak_kind": "measured in this run: 64 pinned blob copies"},
+        "clocks": clk.summary(), "wall_s": t_wall,
+    }), flush=True)
+    st.close()
+
+
 # ---------------------------------------------------------------- GPU arm
 
 def main():
@@ -164,7 +442,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="80b-dec", choices=["80b-dec", "35b-dec"])
+    ap.add_argument("--workload", default="80b-dec", choices=["80b-dec", "35b-dec", "80b-prefill", "80b-stack"])
     ap.add_argument("--tokens", type=int, default=1000, help="decode tokens per bench step")
     ap.add_argument("--replicas", type=int, default=0, help="layer copies to rotate through (0 = >= 3x L2)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -179,6 +457,10 @@ def main():
 
     if args.impl == "reference":
         run_reference(args, shape, rank)
+        return
+    if shape.name in ("80b-prefill", "80b-stack"):
+        if rank == 0:  # single-GPU workloads: other ranks have nothing to do
+            (run_prefill if shape.name == "80b-prefill" else run_stack)(args, shape)
         return
 
     from int4_routed_expert_06_b300 import binding as B
@@ -277,22 +559,15 @@ def main():
             dist.destroy_process_group()
         return
 
-    # ---- roofline of the layer step.  Its three kernels (router, gate/up
-    # SwiGLU, down + combine) overlap under programmatic dependent launch, so
-    # the unit timed is one whole layer call: the event-timed replays divided
-    # by the calls they contain.
+    # ---- roofline of the layer step.  Its two kernels (router; experts:
+    # top-k, gate/up SwiGLU, down + combine) overlap under programmatic
+    # dependent launch, so the unit timed is one whole layer call: the
+    # event-timed replays divided by the calls they contain.
     peak, peak_kind = peaks()
     mean_us = ms * 1e3 / (args.steps * T)
     achieved = per_token / (mean_us * 1e-6) / 1e9
     step_gbs = achieved
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(prof):
-        try:
-            with open(prof) as f:
-                traffic = json.load(f).get(args.workload)
-        except Exception:
-            traffic = None
+    traffic = recorded_traffic(args.workload)
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -304,17 +579,19 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "s32/f32", "data": "synthetic",
+        "dtype_note": "int4 codes x 16-bit fixed-point activations in dp4a (s32), group scales and sums in f32; "
+                      "bf16 x in, bf16 y out",
         "config": {"workload": workload_desc(shape), "tokens_per_step": T, "parallelism": f"replicas{world}",
                    "l2": f"inputs larger than L2: tokens rotate through {R} full layer copies "
                          f"({R * dl.stride * dl.n_slots / 1e9:.1f} GB; the weights {R} tokens touch are "
                          f"{R * (per_token + router_bytes) / 1e6:.0f} MB vs the {l2 / 1e6:.0f} MB L2)",
-                   "graph": "one CUDA graph per step (route + experts calls per token)"},
+                   "graph": "one CUDA graph per step (one moe_layer_forward per token)"},
         "active_expert_bytes_per_token": per_token,
         "hbm": {"achieved_gbs_step": step_gbs, "frac_measured_step": step_gbs / peak,
                 "frac_nominal_8tbs_step": step_gbs / NOMINAL_HBM_GBS},
-        "roofline": {"kernel": "decode layer call: router + gate/up SwiGLU + down/combine kernels, PDL-chained "
-                               "(timed as one unit)",
+        "roofline": {"kernel": "decode layer call: router_tok_kernel + experts_tok_kernel (top-k, gate/up "
+                               "SwiGLU, grid barrier, down + combine), PDL-chained, timed as one unit",
                      "bound": "hbm",
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "mean_us": mean_us,

@@ -97,6 +97,8 @@ cudaError_t launch_router(const Shape &s, const void *x, int T, const void *w_ro
                           const float *bias, const void *w_sg, float *logits, float *sg_logit,
                           cudaStream_t st)
 {
+    if (router_gemm_eligible(s, T))
+        return launch_router_gemm(s, x, T, w_router, bias, w_sg, logits, sg_logit, st);
     if (s.act == MOE_BF16 && s.router == MOE_BF16)
         return router_dispatch<__nv_bfloat16, __nv_bfloat16>(s, x, T, w_router, bias, w_sg, logits, sg_logit, st);
     if (s.act == MOE_F32 && s.router == MOE_F32)

@@ -2,6 +2,7 @@
 // __device__ variable shared by every kernel, so all sources compile together.
 #include "api.cu"
 #include "kernels_decode.cu"
+#include "router_gemm.cu"
 #include "kernels_token.cu"
 #include "prefill.cu"
 #include "bucket.cu"

@@ -16,7 +16,7 @@ import torch
 from gpu_util import assert_close, near_tie_tokens
 from int4_routed_expert_06_b300 import binding as B
 from int4_routed_expert_06_b300 import synth
-from int4_routed_expert_06_b300.stack import PooledStack
+from int4_routed_expert_06_b300.stack import PooledStack, layer_input
 from oracle import oracle as O
 from oracle.slot_policy import SlotPolicy
 
@@ -46,8 +46,9 @@ def test_pool_stack_bit_identical_to_resident_and_policy_exact(stack):
     ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
     checked = 0
     for step in range(24):
-        x = synth.make_x(SHAPE, synth.STACK_X_SEED0 + step, 1, device="cuda")
+        h = synth.make_x(SHAPE, synth.STACK_X_SEED0 + step, 1, device="cuda")
         for l in range(L):
+            x = layer_input(h)
             y = torch.empty((1, SHAPE.hidden), dtype=torch.bfloat16, device="cuda")
             y32 = torch.empty((1, SHAPE.hidden), device="cuda")
             idx = torch.empty((1, k), dtype=torch.int32, device="cuda")
@@ -72,7 +73,7 @@ def test_pool_stack_bit_identical_to_resident_and_policy_exact(stack):
                     np.testing.assert_array_equal(idx.cpu().numpy(), ref["idx"])
                     assert_close(y32.cpu().numpy(), ref["y"], "bf16", f"step {step} layer {l}")
                     checked += 1
-            x = (x.float() + y.float()).to(torch.bfloat16)    # residual chain into the next layer
+            h = (h.float() + y.float()).to(torch.bfloat16)    # residual stream into the next layer
     assert checked >= 6
     s = st.stats()
     assert (s["hits"], s["misses"], s["evictions"]) == (policy.hits, policy.misses, policy.evictions)
