@@ -52,9 +52,8 @@ constexpr int kRec = 80;                             // bytes per fixed-point ch
 constexpr int kExThreads = 512;
 constexpr int kMaxSeg = 2;                           // gate/up segments per CTA
 constexpr int kMaxUnits = 8;                         // gate/up units (8 row pairs) per CTA
-constexpr int kParts = 2;                            // row parts per segment, one barrier each
+constexpr int kParts = 1;                            // row parts per segment, one barrier each
 constexpr int kRowsPerWarp = 4;                      // gate/up row pairs per warp
-constexpr int kDsPer = 2;                            // down scale pieces per thread
 
 // ------------------------------------------------------------ PTX helpers
 
@@ -621,7 +620,7 @@ __device__ __forceinline__ float arec_term(uint4 q, uint4 he, uint4 le, uint4 ho
 // H = 1024 * NXC; TS = scale/bias type.  One CTA of kExThreads per SM.
 //
 // Shared memory (dynamic): per segment [n gate code rows][n up code rows]
-// [n gate scale rows][n up scale rows][n gate bias rows][n up bias rows];
+// [n gate scale rows][n gate bias rows][n up scale rows][n up bias rows];
 // then per active expert its down rows (codes [nr][I_i/2], scales and biases
 // [nr][I_i/G] each); then the partial sums of the down phase.
 template <int NXC, typename TS>
@@ -648,6 +647,8 @@ __global__ void __maxnreg__(112) experts_tok_kernel(ExpertsArgs A)
     const int HG = H >> A.log2G;                     // groups per gate/up row
     const uint32_t qrow = H / 2;                     // code bytes per gate/up row
     const uint32_t sb = sizeof(TS);
+    const uint32_t srow = (uint32_t)HG * sb;         // scale (or bias) bytes per gate/up row
+    const uint32_t rowb = 2 * qrow + 4 * srow;       // shared bytes per row pair of a segment
     const int NU = (A.Is >> 3) + k * (A.I >> 3);
     const int NC = (A.Is >> 5) + k * (A.I >> 5);
     const int u0 = (int)((long)c * NU / n), u1 = (int)((long)(c + 1) * NU / n);
@@ -665,38 +666,49 @@ __global__ void __maxnreg__(112) experts_tok_kernel(ExpertsArgs A)
             seg_o0[nseg] = o0;
             seg_n[nseg] = 8 * len;
             seg_off[nseg] = off;
-            off += (uint32_t)(8 * len) * (2 * qrow);
+            off += (uint32_t)(8 * len) * rowb;
             ++nseg;
             u += len;
         }
     }
     const int NR = 8 * (u1 - u0); // row pairs of this CTA
-    unsigned char *down = smem + (nseg ? seg_off[nseg - 1] + (uint32_t)seg_n[nseg - 1] * (2 * qrow) : 0u);
+    unsigned char *down = smem + (nseg ? seg_off[nseg - 1] + (uint32_t)seg_n[nseg - 1] * rowb : 0u);
     const int h0 = (int)((long)c * (long)H / n), h1 = (int)((long)(c + 1) * (long)H / n);
     const int nr = h1 - h0;
 
     // The copy warp (the last one; it computes no gate/up rows, since a bulk
-    // copy holds its issuing thread until the copy engine takes it): lane
-    // 2 (s kParts + p) + h copies the gate (h = 0) or up (h = 1) code rows of
-    // part p of segment s (rows [p n / kParts, (p + 1) n / kParts)); the h = 0
-    // lane arms the part's barrier first.  Only segments with `pick` set.
-    auto stage_codes = [&](bool (*pick)(int, int), const char *const *base) {
-        const int q = lane >> 1, h = lane & 1, s = q / kParts, p = q - s * kParts;
-        const bool on = s < nseg && pick(seg_i[s], k) && base[s] != nullptr;
-        uint32_t bytes = 0;
-        int r0 = 0;
-        if (s < nseg) {
-            r0 = p * seg_n[s] / kParts;
-            bytes = (uint32_t)((p + 1) * seg_n[s] / kParts - r0) * qrow;
+    // copy holds its issuing thread until the copy engine takes it) stages
+    // part p of segment s (rows [r0, r1) = [p n / kParts, (p + 1) n / kParts))
+    // with lanes 6 (s kParts + p) + j: j < 4 copies those rows of the gate
+    // scales, gate biases, up scales, up biases (small, so issued first),
+    // j = 4 / 5 the gate / up code rows; lane j = 0 arms the part's barrier.
+    // Only segments with `pick` set.
+    auto stage_rows = [&](bool (*pick)(int, int), const char *const *base) {
+        const int q = lane / 6, j = lane - 6 * q, s = q / kParts, p = q - s * kParts;
+        const bool valid = q < kMaxSeg * kParts && s < nseg && pick(seg_i[s], k);
+        const bool on = valid && base[s] != nullptr;
+        uint32_t r0 = 0, nrow = 0;
+        if (valid) {
+            r0 = (uint32_t)(p * seg_n[s] / kParts);
+            nrow = (uint32_t)((p + 1) * seg_n[s] / kParts) - r0;
         }
-        if (s < nseg && pick(seg_i[s], k) && h == 0 && bytes)
-            mbar_expect_tx(&sbar[s][p], on ? 2 * bytes : 0u);
+        if (valid && j == 0 && nrow)
+            mbar_expect_tx(&sbar[s][p], on ? nrow * rowb : 0u);
         __syncwarp();
-        if (on && bytes) {
+        if (on && nrow) {
             const size_t *offs = (seg_i[s] == k) ? A.src.off_sh : A.src.off;
-            const uint32_t nq = (uint32_t)seg_n[s] * qrow;
-            bulk_g2s(smem + seg_off[s] + h * nq + r0 * qrow,
-                     base[s] + offs[h ? M_QU : M_QG] + (size_t)(seg_o0[s] + r0) * qrow, bytes, &sbar[s][p]);
+            const uint32_t nn = (uint32_t)seg_n[s];
+            unsigned char *d = smem + seg_off[s];
+            const size_t row = (size_t)(seg_o0[s] + (int)r0);
+            if (j < 4) {
+                const int m = j == 0 ? M_SG : j == 1 ? M_BG : j == 2 ? M_SU : M_BU;
+                bulk_g2s(d + 2 * nn * qrow + j * nn * srow + r0 * srow, base[s] + offs[m] + row * srow, nrow * srow,
+                         &sbar[s][p]);
+            } else {
+                const int h = j - 4;
+                bulk_g2s(d + h * nn * qrow + r0 * qrow, base[s] + offs[h ? M_QU : M_QG] + row * qrow, nrow * qrow,
+                         &sbar[s][p]);
+            }
         }
     };
 
@@ -725,7 +737,7 @@ __global__ void __maxnreg__(112) experts_tok_kernel(ExpertsArgs A)
     // the shared expert's units come first in the list: stage them now
     if (warp == NW - 1) {
         const char *base[kMaxSeg] = {A.src.shared, A.src.shared};
-        stage_codes([](int i, int kk) { return i == kk; }, base);
+        stage_rows([](int i, int kk) { return i == kk; }, base);
     }
 
     // ---- after the wait: x records and the shared-gate logit are fetched
@@ -741,66 +753,36 @@ __global__ void __maxnreg__(112) experts_tok_kernel(ExpertsArgs A)
             s_base[lane] = routed_base(A.src, tab, s_idx[lane]);
     }
     __syncthreads();
-    // the copy warp: routed code rows, then expert i's down code rows by lane
-    // 8 + i (lane 8 arms the barrier)
+    // the copy warp: routed gate/up rows; then, once every gate/up part of
+    // this SM has landed (the down rows are needed only after the grid
+    // barrier, so they must not compete with the gate/up stream), lane 12 + i
+    // copies expert i's down code, scale and bias rows [h0, h1) (lane 12 arms
+    // the barrier)
     if (warp == NW - 1) {
         const char *base[kMaxSeg];
         for (int s = 0; s < kMaxSeg; ++s)
             base[s] = s < nseg ? s_base[seg_i[s]] : nullptr;
-        stage_codes([](int i, int kk) { return i != kk; }, base);
-        const int i = lane - 8;
+        stage_rows([](int i, int kk) { return i != kk; }, base);
+        for (int s = 0; s < nseg; ++s)
+            for (int p = 0; p < kParts; ++p)
+                if ((p + 1) * seg_n[s] / kParts > p * seg_n[s] / kParts)
+                    mbar_wait0(&sbar[s][p]);
+        const int i = lane - 12;
         const char *b = (i >= 0 && i < n_act) ? s_base[i] : nullptr;
-        const uint32_t nq = b ? (uint32_t)nr * s_qb[i] : 0u;
-        const uint32_t tot = __reduce_add_sync(0xFFFFFFFFu, nq);
-        if (lane == 8)
+        const uint32_t nq = b ? (uint32_t)nr * s_qb[i] : 0u, ns = b ? (uint32_t)(nr * s_ng[i]) * sb : 0u;
+        const uint32_t tot = __reduce_add_sync(0xFFFFFFFFu, nq + 2 * ns);
+        if (lane == 12)
             mbar_expect_tx(&dbar, tot);
         __syncwarp();
-        if (b && nq)
-            bulk_g2s(down + s_eoff[i], b + (i == k ? A.src.off_sh : A.src.off)[M_QD] + (size_t)h0 * s_qb[i], nq,
-                     &dbar);
-    }
-    // scale and bias values by plain loads, issued with the copies: each
-    // lane's group of its warp's gate/up rows (in registers), and this CTA's
-    // rows of every expert's down scales and biases (stored before the grid
-    // barrier)
-    constexpr int NWC = NW - 1; // gate/up warps
-    float gsc[kRowsPerWarp][4]; // gate scale, gate bias, up scale, up bias
-#pragma unroll
-    for (int t = 0; t < kRowsPerWarp; ++t) {
-        const int rp = warp < NWC ? warp + t * NWC : NR;
-        gsc[t][0] = gsc[t][1] = gsc[t][2] = gsc[t][3] = 0.f;
-        if (rp < NR) {
-            const int s = (nseg > 1 && rp >= seg_n[0]) ? 1 : 0, r = s ? rp - seg_n[0] : rp;
-            const char *b = s_base[seg_i[s]];
-            if (b) {
-                const size_t *offs = (seg_i[s] == k) ? A.src.off_sh : A.src.off;
-                const size_t ro = (size_t)(seg_o0[s] + r) * HG + (NXC * lane * 32 >> A.log2G);
-                gsc[t][0] = ld_sb(reinterpret_cast<const TS *>(b + offs[M_SG]) + ro);
-                gsc[t][1] = ld_sb(reinterpret_cast<const TS *>(b + offs[M_BG]) + ro);
-                gsc[t][2] = ld_sb(reinterpret_cast<const TS *>(b + offs[M_SU]) + ro);
-                gsc[t][3] = ld_sb(reinterpret_cast<const TS *>(b + offs[M_BU]) + ro);
-            }
-        }
-    }
-    // down scale/bias pieces: routed expert i owns pieces [i pr, (i+1) pr),
-    // the shared expert the next ps; the first half of an expert's pieces
-    // are scale rows, the second half bias rows
-    const int pr = 2 * nr * s_ng[0] * (int)sb / 16, ps = 2 * nr * s_ng[k] * (int)sb / 16;
-    uint4 dv[kDsPer];
-    int dp[kDsPer];
-#pragma unroll
-    for (int u = 0; u < kDsPer; ++u) {
-        const int P = threadIdx.x + u * kExThreads;
-        const int i = P < k * pr ? P / pr : k, q = P < k * pr ? P - i * pr : P - k * pr, np = i < k ? pr : ps;
-        dp[u] = -1;
-        if (q < np && s_base[i]) {
+        if (b && nq) {
             const size_t *offs = (i == k) ? A.src.off_sh : A.src.off;
-            const int a = q >= np / 2, off = (q - a * (np / 2)) * 16;
-            dv[u] = __ldg(reinterpret_cast<const uint4 *>(s_base[i] + offs[a ? M_BD : M_SD] +
-                                                          (size_t)h0 * s_ng[i] * sb + off));
-            dp[u] = (int)s_eoff[i] + nr * s_qb[i] + a * nr * s_ng[i] * (int)sb + off;
+            unsigned char *d = down + s_eoff[i];
+            bulk_g2s(d, b + offs[M_QD] + (size_t)h0 * s_qb[i], nq, &dbar);
+            bulk_g2s(d + nq, b + offs[M_SD] + (size_t)h0 * s_ng[i] * sb, ns, &dbar);
+            bulk_g2s(d + nq + ns, b + offs[M_BD] + (size_t)h0 * s_ng[i] * sb, ns, &dbar);
         }
     }
+    constexpr int NWC = NW - 1; // gate/up warps
 
     // ---- gate/up: warp w < NWC computes row pairs w, w + NWC, ...
     if (!__all_sync(0xFFFFFFFFu, mbar_wait0(&xbar)))
@@ -827,6 +809,9 @@ __global__ void __maxnreg__(112) experts_tok_kernel(ExpertsArgs A)
         if (s_base[seg_i[s]]) {
             const uint32_t nq = (uint32_t)seg_n[s] * qrow;
             const unsigned char *d = smem + seg_off[s];
+            // this lane's group of row r: gate scale, gate bias, up scale, up bias
+            const TS *sc = reinterpret_cast<const TS *>(d + 2 * nq) + r * HG + ((NXC * lane * 32) >> A.log2G);
+            const int na = seg_n[s] * HG;
             const uint4 *qg = reinterpret_cast<const uint4 *>(d + (size_t)r * qrow);
             const uint4 *qu = reinterpret_cast<const uint4 *>(d + nq + (size_t)r * qrow);
             int dg[NXC], du[NXC];
@@ -843,8 +828,8 @@ __global__ void __maxnreg__(112) experts_tok_kernel(ExpertsArgs A)
                 Du = fmaf((float)du[m], xv[m].sx, Du);
                 Xs += xv[m].X;
             }
-            g = fmaf(gsc[t][0], Dg, gsc[t][1] * Xs);
-            u = fmaf(gsc[t][2], Du, gsc[t][3] * Xs);
+            g = fmaf(to_f32(sc[0]), Dg, to_f32(sc[na]) * Xs);
+            u = fmaf(to_f32(sc[2 * na]), Du, to_f32(sc[3 * na]) * Xs);
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -854,10 +839,6 @@ __global__ void __maxnreg__(112) experts_tok_kernel(ExpertsArgs A)
         if (lane == 0)
             s_a[rp] = g * sigmoid_f(g) * u;
     }
-#pragma unroll
-    for (int uu = 0; uu < kDsPer; ++uu)
-        if (dp[uu] >= 0)
-            *reinterpret_cast<uint4 *>(down + dp[uu]) = dv[uu];
     __syncthreads();
     // each unit writes its quarter of a chunk's record, in kRep copies
     if (threadIdx.x < u1 - u0) {
@@ -1026,7 +1007,7 @@ static int n_chunks(const Shape &s) { return s.Is / 32 + s.k * (s.I / 32); }
 static size_t experts_smem(const Shape &s, int n)
 {
     const size_t sb = s.qscale == MOE_F16 ? 2 : 4;
-    const size_t rowpair = (size_t)s.H; // gate and up code rows
+    const size_t rowpair = (size_t)s.H + 4 * (size_t)(s.H / s.G) * sb; // gate and up code, scale and bias rows
     const int units = (n_units(s) + n - 1) / n;
     const int nr = (s.H + n - 1) / n;
     size_t w = 0;
@@ -1066,9 +1047,7 @@ bool eligible(const Shape &s)
         return false;
     if (8 * units > kRowsPerWarp * (kExThreads / 32 - 1)) // gate/up row pairs per warp
         return false;
-    if (8 + s.k + 1 > 32 || 2 * kMaxSeg * kParts > 8) // lanes of the copy warp
-        return false;
-    if (2 * nr * ((s.k * (s.I / s.G) + s.Is / s.G) * sb) / 16 > kDsPer * kExThreads) // down scale pieces
+    if (12 + s.k + 1 > 32 || 6 * kMaxSeg * kParts > 12) // lanes of the copy warp
         return false;
     return experts_smem(s, n) <= kSmemLimit;
 }
