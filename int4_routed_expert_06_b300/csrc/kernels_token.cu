@@ -784,60 +784,79 @@ __global__ void __maxnreg__(112) experts_tok_kernel(ExpertsArgs A)
     }
     constexpr int NWC = NW - 1; // gate/up warps
 
-    // ---- gate/up: warp w < NWC computes row pairs w, w + NWC, ...
+    // ---- gate/up: warp w < NWC computes row pairs w, w + NWC, ... (at most
+    // kRowsPerWarp).  Every row's dot products come first, with no wait
+    // between rows, so that their loads and dp4a chains overlap; then one
+    // transposing reduction sums all 2 kRowsPerWarp partial values across
+    // the warp (9 shuffles instead of 10 per row).
+    static_assert(kRowsPerWarp == 4 && kParts == 1, "the reduction below assumes 4 rows per warp, 1 part");
     if (!__all_sync(0xFFFFFFFFu, mbar_wait0(&xbar)))
         return;
+    // lane l owns chunks NXC l ... of a row; with two chunks, lanes 4-7 of
+    // each quarter warp take them in the other order (xv[m] is chunk
+    // 2 l + (m ^ sw)), which makes each 16-byte code load conflict-free
+    const int sw = NXC == 2 ? (lane >> 2) & 1 : 0;
     Chunk xv[NXC];
+    float Xs = 0.f; // sum of this lane's x columns (its quantisation group)
 #pragma unroll
-    for (int m = 0; m < NXC; ++m)
-        xv[m] = load_chunk(xs + (size_t)(NXC * lane + m) * kRec);
-    uint32_t waited = 0; // bit s kParts + p: part p of segment s has landed
+    for (int m = 0; m < NXC; ++m) {
+        xv[m] = load_chunk(xs + (size_t)(NXC * lane + (m ^ sw)) * kRec);
+        Xs += xv[m].X;
+    }
+    bool landed = warp < NWC;
+    if (landed)
+        for (int s = 0; s < nseg; ++s)
+            landed &= mbar_wait0(&sbar[s][0]);
+    landed = __all_sync(0xFFFFFFFFu, landed);
+    float v[2 * kRowsPerWarp]; // gate, up partial sums of rows t = 0, 1, ...
 #pragma unroll
     for (int t = 0; t < kRowsPerWarp; ++t) {
-        const int rp = warp < NWC ? warp + t * NWC : NR;
-        if (rp >= NR)
-            break;
-        const int s = (nseg > 1 && rp >= seg_n[0]) ? 1 : 0, r = s ? rp - seg_n[0] : rp;
-        const int p = ((r + 1) * kParts - 1) / seg_n[s]; // part of row r
-        const uint32_t bit = 1u << (s * kParts + p);
-        if (!(waited & bit)) {
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait0(&sbar[s][p])))
-                return;
-            waited |= bit;
-        }
+        const int rp = warp + t * NWC;
         float g = 0.f, u = 0.f;
-        if (s_base[seg_i[s]]) {
-            const uint32_t nq = (uint32_t)seg_n[s] * qrow;
-            const unsigned char *d = smem + seg_off[s];
-            // this lane's group of row r: gate scale, gate bias, up scale, up bias
-            const TS *sc = reinterpret_cast<const TS *>(d + 2 * nq) + r * HG + ((NXC * lane * 32) >> A.log2G);
-            const int na = seg_n[s] * HG;
-            const uint4 *qg = reinterpret_cast<const uint4 *>(d + (size_t)r * qrow);
-            const uint4 *qu = reinterpret_cast<const uint4 *>(d + nq + (size_t)r * qrow);
-            int dg[NXC], du[NXC];
+        if (landed && rp < NR) {
+            const int s = (nseg > 1 && rp >= seg_n[0]) ? 1 : 0, r = s ? rp - seg_n[0] : rp;
+            if (s_base[seg_i[s]]) {
+                const uint32_t nq = (uint32_t)seg_n[s] * qrow;
+                const unsigned char *d = smem + seg_off[s];
+                // this lane's group of row r: gate scale, gate bias, up scale, up bias
+                const TS *sc = reinterpret_cast<const TS *>(d + 2 * nq) + r * HG + ((NXC * lane * 32) >> A.log2G);
+                const int na = seg_n[s] * HG;
+                const uint4 *qg = reinterpret_cast<const uint4 *>(d + (size_t)r * qrow);
+                const uint4 *qu = reinterpret_cast<const uint4 *>(d + nq + (size_t)r * qrow);
+                // one quantisation group per lane: sum_m s (sx_m D_m) + b X_m
+                float Dg = 0.f, Du = 0.f;
 #pragma unroll
-            for (int m = 0; m < NXC; ++m) {
-                dg[m] = chunk_idot(qg[NXC * lane + m], xv[m]);
-                du[m] = chunk_idot(qu[NXC * lane + m], xv[m]);
+                for (int m = 0; m < NXC; ++m) {
+                    Dg = fmaf((float)chunk_idot(qg[NXC * lane + (m ^ sw)], xv[m]), xv[m].sx, Dg);
+                    Du = fmaf((float)chunk_idot(qu[NXC * lane + (m ^ sw)], xv[m]), xv[m].sx, Du);
+                }
+                g = fmaf(to_f32(sc[0]), Dg, to_f32(sc[na]) * Xs);
+                u = fmaf(to_f32(sc[2 * na]), Du, to_f32(sc[3 * na]) * Xs);
             }
-            // one quantisation group per lane: sum_m s (sx_m D_m) + b X_m
-            float Dg = 0.f, Du = 0.f, Xs = 0.f;
-#pragma unroll
-            for (int m = 0; m < NXC; ++m) {
-                Dg = fmaf((float)dg[m], xv[m].sx, Dg);
-                Du = fmaf((float)du[m], xv[m].sx, Du);
-                Xs += xv[m].X;
-            }
-            g = fmaf(to_f32(sc[0]), Dg, to_f32(sc[na]) * Xs);
-            u = fmaf(to_f32(sc[2 * na]), Du, to_f32(sc[3 * na]) * Xs);
         }
+        v[2 * t] = g;
+        v[2 * t + 1] = u;
+    }
+    // round with half-count w: lanes with bit 4 w set keep values [w, 2 w),
+    // the others [0, w), each adding its partner's copy of the kept values
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            g += __shfl_xor_sync(0xFFFFFFFFu, g, o);
-            u += __shfl_xor_sync(0xFFFFFFFFu, u, o);
+    for (int w = kRowsPerWarp; w >= 1; w >>= 1) {
+        const bool hi = (lane & (4 * w)) != 0;
+#pragma unroll
+        for (int j = 0; j < w; ++j) {
+            const float send = hi ? v[j] : v[j + w];
+            const float keep = hi ? v[j + w] : v[j];
+            v[j] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 4 * w);
         }
-        if (lane == 0)
-            s_a[rp] = g * sigmoid_f(g) * u;
+    }
+    v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], 2);
+    v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], 1);
+    // lane l now holds the total of value 2 t + h, t = (l >> 3) & 3, h = (l >> 2) & 1
+    const float up = __shfl_xor_sync(0xFFFFFFFFu, v[0], 4);
+    if ((lane & 7) == 0 && warp < NWC) {
+        const int rp = warp + (lane >> 3) * NWC;
+        if (rp < NR)
+            s_a[rp] = v[0] * sigmoid_f(v[0]) * up;
     }
     __syncthreads();
     // each unit writes its quarter of a chunk's record, in kRep copies
