@@ -56,6 +56,19 @@ if ROOT not in sys.path:
 from int4_routed_expert_06_b300 import synth  # noqa: E402
 
 METRIC = "routed-MoE layer tokens/s (decode, 512e top-10 int4); HBM GB/s vs peak"
+
+
+def metric_of(shape) -> str:
+    """The metric a workload's line reports (METRIC for the 80B decode layer)."""
+    if shape.name == "80b-prefill":
+        return (f"routed-MoE layer prefill tokens/s ({shape.tokens} tokens, {shape.n_experts}e "
+                f"top-{shape.top_k} int4, Zipf-skewed routing)")
+    if shape.name == "80b-stack":
+        return "80B-stack decode tokens/s through a bounded HBM expert pool (25% of experts per layer)"
+    return f"routed-MoE layer tokens/s (decode, {shape.n_experts}e top-{shape.top_k} int4); HBM GB/s vs peak"
+
+
+assert metric_of(synth.DEC_80B) == METRIC
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6400.0
 KERNELS_PER_TOKEN = 2  # single-token path: router (+ x records), experts (top-k, gate/up SwiGLU, down + combine)
@@ -90,9 +103,16 @@ def recorded_traffic(workload: str):
 
 
 def workload_desc(shape) -> str:
+    if shape.name == "80b-prefill":
+        mode = f"{shape.tokens}-token prefill, Zipf(s={shape.zipf_s}) router bias"
+    elif shape.name == "80b-stack":
+        mode = (f"{shape.layers}-layer stack, {shape.pool_slots} pool slots per layer, "
+                f"Zipf(s={shape.zipf_s}) router bias, batch-1 decode")
+    else:
+        mode = "batch-1 decode"
     return (f"{shape.name}: routed MoE layer H={shape.hidden} E={shape.n_experts} top-{shape.top_k} "
             f"I={shape.inter} shared I={shape.shared_inter} sigmoid-gated, int4 affine g{shape.group} "
-            f"{shape.qscale} scale/bias, {shape.act} x/y, batch-1 decode")
+            f"{shape.qscale} scale/bias, {shape.act} x/y, {mode}")
 
 
 # ---------------------------------------------------------------- clocks
@@ -187,7 +207,7 @@ def run_reference(args, shape, rank):
     # rate divided by the layer count (layer 0's weights stand for all)
     v = args.steps / dt / max(shape.layers, 1)
     print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1,
+        "impl": "reference", "metric": metric_of(shape), "value": v, "unit": "tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / max(args.steps, 1) * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": workload_desc(shape), "tokens_per_step": 1,
@@ -265,7 +285,7 @@ def run_prefill(args, shape):
     torch.cuda.synchronize()
     e2e = n_e2e * T / (e0.elapsed_time(e1) * 1e-3)
     print(json.dumps({
-        "metric": "routed-MoE layer prefill tokens/s (4096 tokens, 512e top-10 int4, Zipf-skewed routing)",
+        "metric": metric_of(shape),
         "value": T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16 MMA (f32 accumulate in TMEM)", "data": "synthetic",
@@ -405,7 +425,7 @@ def run_stack(args, shape):
     K = args.steps
     lookups = max(d["hits"] + d["misses"], 1)
     print(json.dumps({
-        "metric": "80B-stack decode tokens/s through a bounded HBM expert pool (25% of experts per layer)",
+        "metric": metric_of(shape),
         "value": K / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "s32/f32", "data": "synthetic",
@@ -577,7 +597,7 @@ def main():
                          "single-threaded C, fp64)"}
 
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "metric": metric_of(shape), "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "s32/f32", "data": "synthetic",
         "dtype_note": "int4 codes x 16-bit fixed-point activations in dp4a (s32), group scales and sums in f32; "

@@ -1,0 +1,63 @@
+"""Host-side pieces of the measurement harness and the stack plumbing (no GPU)."""
+import hashlib
+import os
+
+import torch
+
+import bench
+from int4_routed_expert_06_b300 import synth
+from int4_routed_expert_06_b300.stack import layer_input
+
+
+def test_metric_names_follow_the_workload():
+    assert bench.metric_of(synth.DEC_80B) == bench.METRIC
+    assert "256e top-8" in bench.metric_of(synth.DEC_35B)
+    assert "prefill" in bench.metric_of(synth.PREFILL_80B)
+    assert "stack" in bench.metric_of(synth.STACK_80B)
+    assert "prefill" in bench.workload_desc(synth.PREFILL_80B)
+    assert "48-layer" in bench.workload_desc(synth.STACK_80B)
+
+
+def test_prefill_flops_match_the_scope_table():
+    # 4096 tokens of the 80B layer: routed 257.7 + shared 25.8 + router 8.6 GFLOP
+    f = bench.prefill_flops(synth.PREFILL_80B, 4096)
+    assert abs(f / 1e9 - 292.07) < 0.01
+    # linear in T, and the router alone when no expert exists
+    assert bench.prefill_flops(synth.PREFILL_80B, 8) * 512 == f
+
+
+def test_recorded_traffic_needs_the_same_kernel_source(tmp_path, monkeypatch):
+    src = tmp_path / "int4_routed_expert_06_b300" / "csrc"
+    src.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    (src / "kernels_token.cu").write_text("kernel v1\n")
+    digest = hashlib.sha256(b"kernel v1\n").hexdigest()
+    (tmp_path / "profiles" / "decode_layer_traffic.txt").write_text(
+        "# comment\n" f"80b-dec {digest} 1 2 3\n" "35b-dec 00 1 2 4\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.recorded_traffic("80b-dec") == 3
+    assert bench.recorded_traffic("35b-dec") is None        # recorded for another source
+    assert bench.recorded_traffic("80b-prefill") is None    # not recorded
+    (src / "kernels_token.cu").write_text("kernel v2\n")
+    assert bench.recorded_traffic("80b-dec") is None        # source changed since the capture
+
+
+def test_committed_traffic_record_is_well_formed():
+    p = os.path.join(bench.ROOT, "profiles", "decode_layer_traffic.txt")
+    rows = [l.split() for l in open(p) if l.strip() and not l.startswith("#")]
+    assert rows and all(len(r) == 5 for r in rows)
+    for name, digest, router, experts, total in rows:
+        assert len(digest) == 64 and int(router) + int(experts) == int(total)
+
+
+def test_stack_layer_input_is_unit_rms_and_scale_free():
+    g = torch.Generator().manual_seed(3)
+    h = (torch.randn(5, 2048, generator=g) * torch.tensor([0.1, 1.0, 7.0, 300.0, 1e4])[:, None]).to(torch.bfloat16)
+    u = layer_input(h)
+    assert u.dtype == torch.bfloat16 and u.shape == h.shape
+    rms = u.float().pow(2).mean(-1).sqrt()
+    assert torch.allclose(rms, torch.ones(5), atol=1e-2)
+    # the same residual stream scaled by a power of two gives the same input
+    # (up to one bf16 rounding step: eps is not scaled along)
+    u4 = layer_input((h.float() * 4).to(torch.bfloat16))
+    assert torch.allclose(u4.float(), u.float(), rtol=2 ** -7, atol=0)
