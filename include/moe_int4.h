@@ -121,7 +121,11 @@ size_t moe_layer_workspace_bytes(const moe_config *cfg, int32_t T);
  *   topk_idx [T, k] int32: the k largest logits, ties to the lower expert id,
  *   in descending order; topk_w [T, k] fp32: exp(l_r - l_max) / sum over the
  *   k selected; shared_gate_logit [T] fp32 = w_shared_gate . x[t] (NULL iff no
- *   shared expert); logits_out [T, E] fp32 or NULL.  All device pointers. */
+ *   shared expert); logits_out [T, E] fp32 or NULL.  All device pointers.
+ * For T >= 16 with bf16 x and router the logits are one cuBLAS bf16 GEMM
+ * (fp32 accumulation).  The first such call on a device creates the
+ * library's cuBLAS handle, which allocates device memory: make it outside
+ * stream capture.  moe_layer_forward_noalloc never takes this route. */
 moe_status moe_route(const moe_config *cfg, const void *x, int32_t T, const void *w_router,
                      const float *router_bias, const void *w_shared_gate, int32_t *topk_idx,
                      float *topk_w, float *shared_gate_logit, float *logits_out,
@@ -172,7 +176,13 @@ moe_status moe_experts_forward(const moe_config *cfg, const moe_layer *layer, co
                                void *workspace, size_t ws_bytes, cudaStream_t stream);
 
 /* The whole layer: moe_route then moe_experts_forward.  topk_idx_out [T,k]
- * and topk_w_out [T,k] (device, or NULL) receive the routing. */
+ * and topk_w_out [T,k] (device, or NULL) receive the routing.
+ * T = 1 (bf16, shapes the single-token kernels take) runs two kernels
+ * chained by programmatic dependent launch.  The second puts one CTA on every
+ * SM, and its CTAs meet at a grid barrier.  Work on other streams that holds
+ * SMs for long delays that barrier; past 0.2 s it gives up, records
+ * MOE_ERR_TIMEOUT (read it with moe_get_device_error) and y is not valid.
+ * Run the layer on a stream that does not share the GPU with long kernels. */
 moe_status moe_layer_forward(const moe_config *cfg, const moe_layer *layer, const void *x,
                              int32_t T, void *y, float *y_f32, int32_t *topk_idx_out,
                              float *topk_w_out, void *workspace, size_t ws_bytes,
