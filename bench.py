@@ -115,6 +115,23 @@ def workload_desc(shape) -> str:
             f"{shape.qscale} scale/bias, {shape.act} x/y, {mode}")
 
 
+# ---------------------------------------------------------------- ranks
+
+def max_over_ranks(x: float, dist=None, device: str = "cuda") -> float:
+    """The largest x over all ranks of the process group (x itself without
+    one): the job's time is its slowest replica's."""
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank * world / (ms_max / 1e3)
+
+
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -543,12 +560,8 @@ def main():
     ms = start.elapsed_time(end)
     if B.moe_get_device_error(stream) != 0:
         raise RuntimeError("a kernel recorded a device error during the bench")
-    ms_all = torch.tensor([ms], device="cuda")
-    if dist:
-        dist.all_reduce(ms_all, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_all.item())
-    tokens_total = args.steps * T * world
-    value = tokens_total / (ms_max / 1e3)
+    ms_max = max_over_ranks(ms, dist, "cuda")
+    value = job_tokens_per_s(args.steps * T, world, ms_max)
 
     # ---- end to end through the public calls: pinned host x in, pinned host y out
     e2e_steps = min(args.steps, 3)
@@ -568,11 +581,7 @@ def main():
             y_host.copy_(y_dev, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    e2e_all = torch.tensor([e2e_ms], device="cuda")
-    if dist:
-        dist.all_reduce(e2e_all, op=dist.ReduceOp.MAX)
-    e2e_value = e2e_steps * T * world / (float(e2e_all.item()) / 1e3)
+    e2e_value = job_tokens_per_s(e2e_steps * T, world, max_over_ranks(e0.elapsed_time(e1), dist, "cuda"))
 
     if rank != 0:
         if dist:
