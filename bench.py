@@ -599,7 +599,7 @@ def main():
     traffic = recorded_traffic(args.workload)
 
     cpu = None
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:  # the oracle's baseline is an N = 1 figure
         v, n, dt = oracle_tokens_per_s(w, shape, xs, args.cpu_seconds, 400)
         cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"first {n} of the {T} seeded decode tokens of one bench step ({dt:.1f} s, "
