@@ -142,6 +142,10 @@ def _ptr(t) -> Optional[int]:
     if isinstance(t, int):
         return t
     if isinstance(t, torch.Tensor):
+        if not t.is_contiguous():
+            # the C ABI takes dense row-major arrays; a strided view would be
+            # read as if it were dense
+            raise ValueError(f"tensor of shape {tuple(t.shape)} and strides {t.stride()} is not contiguous")
         return t.data_ptr()
     raise TypeError(f"cannot pass {type(t)} as a pointer")
 

@@ -123,3 +123,11 @@ def test_slot_pool_exhaustion_and_fill_mismatch():
             B.slot_pool_lookup(p, 0, [512])
     finally:
         B.slot_pool_destroy(p)
+
+
+def test_strided_tensors_are_refused_before_any_call():
+    import torch
+    cfg = B.config_for(synth.DEC_80B)
+    x = torch.zeros((4, 2 * synth.DEC_80B.hidden), dtype=torch.bfloat16)[:, ::2]
+    with pytest.raises(ValueError):
+        B.moe_layer_forward(cfg, B.moe_layer(), x, 4, None, stream=0)
