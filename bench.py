@@ -16,7 +16,7 @@ R full copies of the layer (R chosen so the rotating working set is at least
 Reported: tokens/s (whole job, all ranks), the layer call's achieved HBM
 bandwidth on algorithmic bytes (active expert bytes over the event-timed
 mean duration of one layer call) against the measured copy peak, the oracle's
-CPU throughput on a bounded sample, and an end-to-end number through the
+CPU throughput on a bounded sample (single-GPU runs), and an end-to-end number through the
 public C-ABI calls with pinned host buffers and copies inside the timed
 region.  Multi-GPU runs are independent replicas (the layer does not shard
 at batch 1); no collective touches the data path.
