@@ -471,6 +471,77 @@ def run_stack(args, shape):
     st.close()
 
 
+# ---------------------------------------------------------------- policy study
+
+POLICY_RULES = {"lfu_recency": 0, "lru": 1, "lfu": 2}  # MOE_POOL_* codes of the C ABI
+
+
+def routing_trace(shape, layer: int, tokens: int):
+    """Top-k expert ids [tokens, k] of one stack layer on unit-RMS Gaussian
+    layer inputs.  The stack's own router weights and Zipf bias (synth's
+    draws for that layer); the inputs stand in for the normalised residual
+    stream, which also has unit RMS per token."""
+    r = synth.make_router(shape, shape.weight_seed + layer, "cpu")
+    g = torch.Generator().manual_seed(9000 + layer)
+    x = torch.randn((tokens, shape.hidden), generator=g)
+    logits = x @ r["w_router"].float().t()
+    if r["router_bias"] is not None:
+        logits = logits + r["router_bias"]
+    return torch.topk(logits, shape.top_k, dim=1).indices.to(torch.int32)
+
+
+def run_policy_study(args):
+    """Hit rate of the slot pool's host policy (the library's own
+    slot_pool_lookup) against pool fraction, Zipf skew and eviction rule, on
+    routing traces of the 80B stack's layers.  Only lookups run: placeholder
+    addresses stand in for the pool and backing store, which a lookup never
+    touches."""
+    import dataclasses
+    from int4_routed_expert_06_b300 import binding as B
+
+    base = synth.STACK_80B
+    E = base.n_experts
+    layers, warm, tokens = 4, 32, max(args.steps, 64)
+    placeholder = 1 << 40  # 256-byte aligned, never dereferenced by a lookup
+    cfg = B.config_for(base)
+    stride = B.moe_blob_layout_get(cfg, base.inter).bytes
+    rows = []
+    t0 = time.perf_counter()
+    for s in (0.0, 0.8, 1.1, 1.4):
+        shape = dataclasses.replace(base, zipf_s=s)
+        traces = [routing_trace(shape, l, warm + tokens).tolist() for l in range(layers)]
+        for frac in (0.10, 0.25, 0.50):
+            slots = int(round(frac * E))
+            for rule, code in POLICY_RULES.items():
+                p = B.slot_pool_create(cfg, layers, slots, placeholder, layers * slots * stride, placeholder,
+                                       stride, side_stream=0)
+                try:
+                    B.slot_pool_set_policy(p, code)
+                    for j in range(warm + tokens):
+                        if j == warm:
+                            s0 = B.slot_pool_stats(p)
+                        for l in range(layers):
+                            B.slot_pool_lookup(p, l, traces[l][j])
+                    s1 = B.slot_pool_stats(p)
+                finally:
+                    B.slot_pool_destroy(p)
+                hits, misses = s1["hits"] - s0["hits"], s1["misses"] - s0["misses"]
+                rows.append({"zipf_s": s, "pool_fraction": frac, "slots": slots, "rule": rule,
+                             "hit_rate": hits / max(hits + misses, 1), "misses_per_token_layer": misses / (tokens * layers)})
+    dt = time.perf_counter() - t0
+    head = next(r for r in rows if r["zipf_s"] == base.zipf_s and r["pool_fraction"] == 0.25
+                and r["rule"] == "lfu_recency")
+    print(json.dumps({
+        "metric": "slot-pool hit rate against pool fraction, Zipf skew and eviction rule (host policy)",
+        "value": head["hit_rate"], "unit": "hit rate", "higher_is_better": True,
+        "steps": tokens, "warmup": warm, "data": "synthetic",
+        "config": {"workload": f"80b-stack routers: E={E} top-{base.top_k}, {layers} layers, {tokens} tokens "
+                               f"after {warm} warm-up tokens, unit-RMS Gaussian layer inputs",
+                   "headline": "pool 25%, Zipf s=1.1, LFU+recency (the stack workload's setting)"},
+        "table": rows, "host_s": dt,
+    }), flush=True)
+
+
 # ---------------------------------------------------------------- GPU arm
 
 def main():
@@ -479,7 +550,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="80b-dec", choices=["80b-dec", "35b-dec", "80b-prefill", "80b-stack"])
+    ap.add_argument("--workload", default="80b-dec",
+                    choices=["80b-dec", "35b-dec", "80b-prefill", "80b-stack", "policy-study"])
     ap.add_argument("--tokens", type=int, default=1000, help="decode tokens per bench step")
     ap.add_argument("--replicas", type=int, default=0, help="layer copies to rotate through (0 = >= 3x L2)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -490,6 +562,10 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.workload == "policy-study":
+        if rank == 0:  # host-only: the pool's eviction rules on routing traces
+            run_policy_study(args)
+        return
     shape = synth.SHAPES[args.workload]
 
     if args.impl == "reference":

@@ -237,6 +237,18 @@ moe_status slot_pool_create(const moe_config *cfg, int32_t n_layers, int32_t slo
                             void *pool_dev, size_t pool_bytes, const void *backing_host,
                             size_t expert_stride, cudaStream_t side_stream, slot_pool **out);
 
+/* Eviction rules a pool can use (all take empty slots first, lowest id
+ * first, and never evict an expert the same lookup needs):
+ *   MOE_POOL_LFU_RECENCY  smallest use count, then oldest stamp, then lowest
+ *                         slot id (the default; the rule the pages name);
+ *   MOE_POOL_LRU          oldest stamp, then lowest slot id;
+ *   MOE_POOL_LFU          smallest use count, then lowest slot id.
+ * Use counts and stamps are kept the same way under every rule.  The rule
+ * may be changed between lookups; it applies to the evictions that follow.
+ * Returns MOE_ERR_INVALID_ARG for an unknown rule. */
+typedef enum { MOE_POOL_LFU_RECENCY = 0, MOE_POOL_LRU = 1, MOE_POOL_LFU = 2 } moe_pool_policy;
+moe_status slot_pool_set_policy(slot_pool *p, int32_t policy);
+
 /* Apply the policy to one lookup of `n` expert ids (host array) of `layer`:
  * hits are stamped, each miss gets a slot (evicting if needed) in the host
  * table.  slots_out [n] (host) receives the slot of every id; miss_ids

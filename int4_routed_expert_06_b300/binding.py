@@ -99,6 +99,7 @@ _SIGS = {
     "moe_pooled_layer_forward": (_I, [_CP(moe_config), _P, _I, _CP(moe_resident_weights), _P, _I, _P, _P, _P,
                                       _P, _Z, _P]),
     "slot_pool_destroy": (None, [_P]),
+    "slot_pool_set_policy": (_I, [_P, _I]),
     "moe_get_device_error": (_I, [_P]),
     "moe_last_error_message": (C.c_char_p, []),
     "moe_version": (C.c_char_p, []),
@@ -276,6 +277,13 @@ def moe_pooled_layer_forward(cfg, pool: int, layer: int, weights: moe_resident_w
     _check(lib().moe_pooled_layer_forward(C.byref(cfg), pool, layer, C.byref(weights), _ptr(x), T, _ptr(y),
                                           _ptr(y_f32), _ptr(topk_idx_out), _ptr(workspace), ws_bytes,
                                           _stream(stream)), "moe_pooled_layer_forward")
+
+
+MOE_POOL_LFU_RECENCY, MOE_POOL_LRU, MOE_POOL_LFU = 0, 1, 2
+
+
+def slot_pool_set_policy(pool: int, policy: int) -> None:
+    _check(lib().slot_pool_set_policy(pool, policy), "slot_pool_set_policy")
 
 
 def slot_pool_destroy(pool: int) -> None:

@@ -10,6 +10,8 @@
 //   miss -> lowest empty slot, else evict the expert not needed by this
 //           lookup with the smallest (use count, stamp, slot id); the filled
 //           slot starts at use count 1.
+// Two comparison rules are selectable for studies (slot_pool_set_policy):
+// LRU, the smallest (stamp, slot id), and LFU, the smallest (use count, slot id).
 #include <mutex>
 #include <vector>
 
@@ -57,6 +59,7 @@ struct slot_pool {
     int64_t clock = 0;
     int32_t *table_dev = nullptr;
     moe_pool_stats st{};
+    int32_t policy = MOE_POOL_LFU_RECENCY;
     std::mutex mu;
     // moe_pooled_layer_forward: pinned readback of the routed ids, scratch
     // lists, and events that time the compute stream's wait for fills.
@@ -191,8 +194,19 @@ extern "C" moe_status slot_pool_lookup(slot_pool *p, int32_t layer, const int32_
                     needed |= (own[j] == u);
                 if (needed)
                     continue;
-                if (s < 0 || fr[j] < fr[s] || (fr[j] == fr[s] && sp[j] < sp[s]))
-                    s = j; // equal (count, stamp): the lower slot id, found first, stays
+                // a candidate replaces the current victim only when its key
+                // is strictly smaller, so on equal keys the lower slot id stays
+                bool smaller = s < 0;
+                if (!smaller) {
+                    if (p->policy == MOE_POOL_LRU)
+                        smaller = sp[j] < sp[s];
+                    else if (p->policy == MOE_POOL_LFU)
+                        smaller = fr[j] < fr[s];
+                    else
+                        smaller = fr[j] < fr[s] || (fr[j] == fr[s] && sp[j] < sp[s]);
+                }
+                if (smaller)
+                    s = j;
             }
             evicted = own[s];
             tab[evicted] = -1;
@@ -210,6 +224,18 @@ extern "C" moe_status slot_pool_lookup(slot_pool *p, int32_t layer, const int32_
     *n_miss = (int32_t)fills.size();
     for (size_t j = 0; j < fills.size(); ++j)
         miss_ids[j] = fills[j].expert;
+    return MOE_OK;
+}
+
+extern "C" moe_status slot_pool_set_policy(slot_pool *p, int32_t policy)
+{
+    using namespace moe;
+    if (!p)
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_set_policy: NULL pool");
+    if (policy != MOE_POOL_LFU_RECENCY && policy != MOE_POOL_LRU && policy != MOE_POOL_LFU)
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_set_policy: unknown policy %d", policy);
+    std::lock_guard<std::mutex> g(p->mu);
+    p->policy = policy;
     return MOE_OK;
 }
 

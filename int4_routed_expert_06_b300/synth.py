@@ -167,6 +167,19 @@ def zipf_router_bias(shape: MoEShape, seed: int, device="cpu") -> Optional[torch
     return bias.to(torch.float32).to(device)
 
 
+def make_router(shape: MoEShape, seed: Optional[int] = None, device="cpu") -> Dict[str, torch.Tensor]:
+    """The resident routing weights of a layer, exactly as make_layer draws
+    them: w_router [E,H], w_shared_gate [H], router_bias [E] fp32 or None."""
+    seed = shape.weight_seed if seed is None else seed
+    gen = _gen(seed, device)
+    rd = torch_dtype(shape.router)
+    return {
+        "w_router": _randn((shape.n_experts, shape.hidden), shape.router_std, gen, device).to(rd),
+        "w_shared_gate": _randn((shape.hidden,), shape.router_std, gen, device).to(rd),
+        "router_bias": zipf_router_bias(shape, seed, device),
+    }
+
+
 def make_layer(shape: MoEShape, seed: Optional[int] = None, device="cpu") -> Dict[str, torch.Tensor]:
     """One layer's stored weights, all in the dtypes the shape names.
 
@@ -175,13 +188,7 @@ def make_layer(shape: MoEShape, seed: Optional[int] = None, device="cpu") -> Dic
     under 'shared_' + key (leading dim 1).
     """
     seed = shape.weight_seed if seed is None else seed
-    gen = _gen(seed, device)
-    rd = torch_dtype(shape.router)
-    layer = {
-        "w_router": _randn((shape.n_experts, shape.hidden), shape.router_std, gen, device).to(rd),
-        "w_shared_gate": _randn((shape.hidden,), shape.router_std, gen, device).to(rd),
-        "router_bias": zipf_router_bias(shape, seed, device),
-    }
+    layer = make_router(shape, seed, device)
     layer.update(make_experts(shape, shape.n_experts, shape.inter, seed * 31 + 1, device))
     if shape.shared_inter > 0:
         sh = make_experts(shape, 1, shape.shared_inter, seed * 31 + 2, device)

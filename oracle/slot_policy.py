@@ -15,6 +15,11 @@ recency"; they do not spell the rule out.  The reading written here:
     the filled slot starts at freq = 1, last_use = clock;
   * a lookup whose distinct needed experts exceed n_slots cannot be served.
 
+Two more victim rules, for policy studies (the pages name only the first):
+  * "lru": the smallest last_use, then the lowest slot id;
+  * "lfu": the smallest freq, then the lowest slot id.
+Use counts and last_use are kept the same way under every rule.
+
 Plain Python, one slot at a time; independent of the C++ policy in the
 library.
 """
@@ -27,8 +32,19 @@ class PoolExhausted(RuntimeError):
     pass
 
 
+# victim order of each rule: the candidate slot with the smallest key is evicted
+_KEYS = {
+    "lfu_recency": lambda fr, la, j: (fr[j], la[j], j),
+    "lru": lambda fr, la, j: (la[j], j),
+    "lfu": lambda fr, la, j: (fr[j], j),
+}
+
+
 class SlotPolicy:
-    def __init__(self, n_layers: int, n_experts: int, n_slots: int):
+    def __init__(self, n_layers: int, n_experts: int, n_slots: int, rule: str = "lfu_recency"):
+        if rule not in _KEYS:
+            raise ValueError(f"unknown rule {rule!r}")
+        self.key = _KEYS[rule]
         self.n_layers, self.n_experts, self.n_slots = n_layers, n_experts, n_slots
         self.table = [[-1] * n_experts for _ in range(n_layers)]
         self.owner = [[-1] * n_slots for _ in range(n_layers)]
@@ -64,7 +80,7 @@ class SlotPolicy:
                 s = empty[0]
             else:
                 cands = [s for s in range(self.n_slots) if own[s] not in uniq]
-                s = min(cands, key=lambda j: (fr[j], la[j], j))
+                s = min(cands, key=lambda j: self.key(fr, la, j))
                 tab[own[s]] = -1
                 self.evictions += 1
             own[s] = e

@@ -1,6 +1,7 @@
 """The C-ABI library on the CPU: it loads, exports every declared symbol,
 validates arguments without touching a GPU, and its host-side pieces (blob
-layout, repack, LFU+recency slot policy) agree with independent versions."""
+layout, repack, the slot policy under each eviction rule) agree with
+independent versions."""
 import ctypes
 import random
 
@@ -80,10 +81,14 @@ def _pool(n_layers, n_slots, shape=synth.DEC_80B):
                               stride, side_stream=0)
 
 
-def test_slot_policy_matches_oracle_on_zipf_traces():
+@pytest.mark.parametrize("rule, code", [("lfu_recency", B.MOE_POOL_LFU_RECENCY), ("lru", B.MOE_POOL_LRU),
+                                        ("lfu", B.MOE_POOL_LFU)])
+def test_slot_policy_matches_oracle_on_zipf_traces(rule, code):
     L, E, S, k = 3, 512, 32, 10
     p = _pool(L, S)
-    ref = SlotPolicy(L, E, S)
+    if code != B.MOE_POOL_LFU_RECENCY:
+        B.slot_pool_set_policy(p, code)
+    ref = SlotPolicy(L, E, S, rule)
     rng = random.Random(0)
     w = [1.0 / (r + 1) ** 1.1 for r in range(E)]
     try:
@@ -102,6 +107,16 @@ def test_slot_policy_matches_oracle_on_zipf_traces():
         st = B.slot_pool_stats(p)
         assert (st["hits"], st["misses"], st["evictions"]) == (ref.hits, ref.misses, ref.evictions)
         assert st["lookups"] == 300 * L and st["bytes_filled"] == 0
+    finally:
+        B.slot_pool_destroy(p)
+
+
+def test_slot_pool_rejects_unknown_policy():
+    p = _pool(1, 4)
+    try:
+        with pytest.raises(B.MoEError) as ei:
+            B.slot_pool_set_policy(p, 3)
+        assert ei.value.status == B.MOE_ERR_INVALID_ARG
     finally:
         B.slot_pool_destroy(p)
 

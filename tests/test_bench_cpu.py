@@ -61,3 +61,24 @@ def test_stack_layer_input_is_unit_rms_and_scale_free():
     # (up to one bf16 rounding step: eps is not scaled along)
     u4 = layer_input((h.float() * 4).to(torch.bfloat16))
     assert torch.allclose(u4.float(), u.float(), rtol=2 ** -7, atol=0)
+
+
+def test_policy_study_runs_the_library_policy_and_uniform_routing_hits_the_pool_fraction(capsys):
+    import argparse
+    import json
+    bench.run_policy_study(argparse.Namespace(steps=64))
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    rows = line["table"]
+    assert len(rows) == 4 * 3 * 3 and 0.0 < line["value"] < 1.0
+    for r in rows:
+        assert 0.0 <= r["hit_rate"] <= 1.0
+        if r["zipf_s"] == 0.0:   # no skew: a pool holding a fraction f of the experts hits about f
+            assert abs(r["hit_rate"] - r["pool_fraction"]) < 0.06, r
+
+
+def test_routing_trace_uses_the_stack_router():
+    shape = synth.STACK_80B
+    t = bench.routing_trace(shape, 0, 8)
+    assert t.shape == (8, shape.top_k) and t.dtype == torch.int32
+    assert all(len(set(row.tolist())) == shape.top_k for row in t)
+    assert int(t.min()) >= 0 and int(t.max()) < shape.n_experts

@@ -223,7 +223,7 @@ def test_slot_policy_golden_traces():
     with open(os.path.join(GOLDEN, "slot_policy_traces.json")) as f:
         traces = json.load(f)["traces"]
     for tr in traces:
-        pol = SlotPolicy(1, tr["n_experts"], tr["n_slots"])
+        pol = SlotPolicy(1, tr["n_experts"], tr["n_slots"], tr.get("rule", "lfu_recency"))
         for st in tr["steps"]:
             before = list(pol.table[0])
             slots, fills = pol.lookup(0, st["need"])
