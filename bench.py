@@ -71,7 +71,7 @@ def metric_of(shape) -> str:
 assert metric_of(synth.DEC_80B) == METRIC
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6400.0
-KERNELS_PER_TOKEN = 2  # single-token path: router (+ x records), experts (top-k, gate/up SwiGLU, down + combine)
+KERNELS_PER_TOKEN = 3  # single-token path: router (+ x records), gate/up (top-k, SwiGLU), down (+ combine)
 
 
 def peaks():
@@ -695,8 +695,8 @@ def main():
         "active_expert_bytes_per_token": per_token,
         "hbm": {"achieved_gbs_step": step_gbs, "frac_measured_step": step_gbs / peak,
                 "frac_nominal_8tbs_step": step_gbs / NOMINAL_HBM_GBS},
-        "roofline": {"kernel": "decode layer call: router_tok_kernel + experts_tok_kernel (top-k, gate/up "
-                               "SwiGLU, grid barrier, down + combine), PDL-chained, timed as one unit",
+        "roofline": {"kernel": "decode layer call: router_tok_kernel + gateup_tok_kernel (top-k, gate/up "
+                               "SwiGLU) + down_tok_kernel (down + combine), PDL-chained, timed as one unit",
                      "bound": "hbm",
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "mean_us": mean_us,

@@ -177,12 +177,11 @@ moe_status moe_experts_forward(const moe_config *cfg, const moe_layer *layer, co
 
 /* The whole layer: moe_route then moe_experts_forward.  topk_idx_out [T,k]
  * and topk_w_out [T,k] (device, or NULL) receive the routing.
- * T = 1 (bf16, shapes the single-token kernels take) runs two kernels
- * chained by programmatic dependent launch.  The second puts one CTA on every
- * SM, and its CTAs meet at a grid barrier.  Work on other streams that holds
- * SMs for long delays that barrier; past 0.2 s it gives up, records
- * MOE_ERR_TIMEOUT (read it with moe_get_device_error) and y is not valid.
- * Run the layer on a stream that does not share the GPU with long kernels. */
+ * T = 1 (bf16, shapes the single-token kernels take) runs three kernels
+ * chained by programmatic dependent launch: router, gate/up (top-k and
+ * SwiGLU), down (weighted combine).  No kernel waits on another kernel's
+ * CTAs, so the call needs no co-residency and cannot stall behind work on
+ * other streams. */
 moe_status moe_layer_forward(const moe_config *cfg, const moe_layer *layer, const void *x,
                              int32_t T, void *y, float *y_f32, int32_t *topk_idx_out,
                              float *topk_w_out, void *workspace, size_t ws_bytes,
@@ -309,12 +308,25 @@ const char *moe_last_error_message(void);
 /* Library version string. */
 const char *moe_version(void);
 
-/* Kernel selection, process-wide: 0 (default) uses the single-token kernels
- * (bulk-copy staged, PDL-chained) for T = 1 and the tcgen05 grouped GEMMs for
- * T >= 64 where the shape allows; 1 forces the generic kernels everywhere.  The two compute the same function
- * (the pages' practice of checking fast against scalar kernels); tests compare
+/* Kernel selection for calls made from the calling host thread (the setting
+ * is per thread): 0 (default) uses the single-token kernels for T = 1 and
+ * the tcgen05 grouped GEMMs for T >= 64 where the shape allows; 1 forces the
+ * generic kernels everywhere.  The two compute the same function (the
+ * pages' practice of checking fast against scalar kernels); tests compare
  * both against the CPU oracle.  MOE_ERR_INVALID_ARG for other values. */
 moe_status moe_set_kernel_path(int32_t path);
+
+/* Test hooks, process-wide, for exercising the failure path of bounded
+ * device waits without a fault: every wait a kernel of this library makes
+ * gives up after wait_ns (default 200,000,000 = 0.2 s) and records
+ * MOE_ERR_TIMEOUT; extra_arrivals (default 0, at most 4) is added to the
+ * arrivals the single-token down kernel's copy barrier expects, so that with
+ * extra_arrivals > 0 that wait always runs out.  After giving up, the kernel
+ * supplies those arrivals itself, waits for its copies to land, writes zeros
+ * for the affected outputs and returns.  Synchronous (cudaMemcpyToSymbol on
+ * the current device); MOE_ERR_INVALID_ARG for wait_ns == 0 or
+ * extra_arrivals outside [0, 4].  Not for production use. */
+moe_status moe_debug_set_waits(uint64_t wait_ns, int32_t extra_arrivals);
 
 #ifdef __cplusplus
 }

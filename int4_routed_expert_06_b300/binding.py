@@ -104,6 +104,7 @@ _SIGS = {
     "moe_last_error_message": (C.c_char_p, []),
     "moe_version": (C.c_char_p, []),
     "moe_set_kernel_path": (_I, [_I]),
+    "moe_debug_set_waits": (_I, [C.c_uint64, _I]),
 }
 
 
@@ -305,6 +306,10 @@ def moe_version() -> str:
 
 def moe_set_kernel_path(path: int) -> None:
     _check(lib().moe_set_kernel_path(path), "moe_set_kernel_path")
+
+
+def moe_debug_set_waits(wait_ns: int, extra_arrivals: int) -> None:
+    _check(lib().moe_debug_set_waits(wait_ns, extra_arrivals), "moe_debug_set_waits")
 
 
 # ------------------------------------------------------------------ marshalling helpers

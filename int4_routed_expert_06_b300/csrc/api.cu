@@ -10,7 +10,7 @@
 namespace moe {
 
 static thread_local char t_msg[512] = "";
-static int g_kernel_path = 0;
+static thread_local int g_kernel_path = 0;
 
 int kernel_path() { return g_kernel_path; }
 
@@ -242,7 +242,7 @@ moe_status moe_route(const moe_config *cfg, const void *x, int32_t T, const void
     cudaError_t e;
     if (T == 1 && tok::eligible(s))
         e = tok::launch_router(s, x, w_router, router_bias, w_shared_gate, logits, 0, 1, shared_gate_logit,
-                               nullptr, 0, nullptr, stream);
+                               nullptr, 0, stream);
     else
         e = launch_router(s, x, T, w_router, router_bias, s.Is > 0 ? w_shared_gate : nullptr, logits,
                           shared_gate_logit, stream);
@@ -385,7 +385,7 @@ moe_status moe_experts_forward(const moe_config *cfg, const moe_layer *L, const 
     if (T == 1 && tok::eligible(s)) {
         const tok::Bufs b = tok::bufs_carve(s, static_cast<char *>(workspace) + w.tok);
         cudaError_t e = tok::launch_router(s, x, nullptr, nullptr, nullptr, nullptr, 0, 0, nullptr, b.xrec, b.xrs,
-                                           b.bar, stream);
+                                           stream);
         if (e != cudaSuccess)
             return cuda_check(e, "moe_experts_forward: x records");
         tok::Routing R{nullptr, 0, topk_idx, topk_w, nullptr, nullptr, shared_gate_logit};
@@ -432,7 +432,7 @@ moe_status moe_layer_forward(const moe_config *cfg, const moe_layer *L, const vo
             return st;
         const tok::Bufs b = tok::bufs_carve(s, ws + w.tok);
         cudaError_t e = tok::launch_router(s, x, L->w_router, L->router_bias, L->w_shared_gate, b.lg, b.lgs,
-                                           tok::kRep, nullptr, b.xrec, b.xrs, b.bar, stream);
+                                           tok::kRep, nullptr, b.xrec, b.xrs, stream);
         if (e != cudaSuccess)
             return cuda_check(e, "moe_layer_forward: router");
         tok::Routing R{b.lg, b.lgs, nullptr, nullptr, idx, tw, nullptr};

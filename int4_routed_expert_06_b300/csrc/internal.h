@@ -69,9 +69,8 @@ struct Bufs {
     int lgs;             // floats per logits copy
     unsigned char *xrec; // [kRep][xrs]: fixed-point records of x
     size_t xrs;          // bytes per x copy
-    unsigned char *arec; // [kRep][ars]: fixed-point records of the 32-row chunks of a
+    unsigned char *arec; // [kRep][ars]: activation records of the 32-row chunks of a
     size_t ars;          // bytes per record copy
-    unsigned int *bar;   // grid barrier counter of the experts kernel
 };
 size_t bufs_bytes(const Shape &s);
 Bufs bufs_carve(const Shape &s, char *base);
@@ -93,12 +92,11 @@ bool eligible(const Shape &s);
 // Router logits (rows skipped when w_router is NULL) into `lg` (lgs floats
 // apart, nrep copies; the shared-gate logit goes to lg[E] of each copy when
 // lgs > 0 and to *sg when sg is non-NULL) and, when xrec is non-NULL, the
-// fixed-point records of x into kRep copies xrs bytes apart; zeroes *bar
-// (the experts kernel's barrier counter) when bar is non-NULL.
+// fixed-point records of x into kRep copies xrs bytes apart.
 cudaError_t launch_router(const Shape &s, const void *x, const void *w_router, const float *bias,
                           const void *w_sg, float *lg, int lgs, int nrep, float *sg, unsigned char *xrec,
-                          size_t xrs, unsigned int *bar, cudaStream_t st);
-// gate/up SwiGLU then down + weighted combine, in one kernel.
+                          size_t xrs, cudaStream_t st);
+// gate/up SwiGLU, then down + weighted combine: two PDL-chained kernels.
 cudaError_t launch_experts(const Shape &s, const Bufs &b, const ExpertSrc &src, const Routing &R, void *y,
                            float *y32, cudaStream_t st);
 } // namespace tok

@@ -1,29 +1,35 @@
 // Single-token (batch-1 decode) path of the routed int4 MoE layer on B300.
 //
-// Two kernels chained with programmatic dependent launch (PDL).  Each kernel
-// loads what does not depend on its predecessor's output (weights, the slot
-// table) before griddepcontrol.wait, and reads its predecessor's outputs and
-// writes its own only after the wait, so a successor never races a kernel
-// that still reads a buffer it is about to overwrite.
+// Three kernels per layer call, chained with programmatic dependent launch
+// (PDL).  Each loads what does not depend on its predecessor's output
+// (weights, the slot table) before griddepcontrol.wait, and reads its
+// predecessor's outputs and writes its own only after the wait, so a
+// successor never races a kernel that still reads a buffer it overwrites.
+// A kernel boundary is the device-wide exchange: on B300 it costs about
+// half of what a 148-CTA grid barrier inside one kernel does, and it needs no
+// co-residency guarantee.
 //
-//   router_tok   one warp per router row (E experts, then the shared-gate
-//                row), the row's bf16 weights held in registers before the
-//                wait; after it, x is read and the logits written (in kRep
-//                copies).  A few extra CTAs convert x into the fixed-point
-//                chunk records the expert kernel uses.
-//   experts_tok  one CTA per SM.  Top-k from the logits (one warp per CTA,
-//                every CTA), then every weight byte the CTA needs is copied
-//                into shared memory at once: its 32-row chunks of the active
-//                experts' gate/up rows and its output rows of their W_d.  It
-//                computes a = silu(W_g x) * (W_u x) for its chunks and writes
-//                each chunk's fixed-point record; after a grid-wide barrier it
-//                reads all records and accumulates
-//                  y[h] = sum_r w_r (W_d,r a_r)[h] + sigmoid(s) (W_d,sh a_sh)[h]
-//                for its output rows in a fixed order.
-//
-// Code on the critical path is kept small and loop-shaped: these kernels run
-// once per token on every SM, and long unrolled stretches stall on
-// instruction fetch.
+//   router_tok  one warp per router row (E experts, then the shared-gate
+//               row), the row's bf16 weights held in registers before the
+//               wait; after it, x is read and the logits written (in kRep
+//               copies).  A few extra CTAs convert x into the fixed-point
+//               chunk records the gate/up kernel uses.
+//   gateup_tok  one CTA of 512 threads per SM.  Before the wait: the slot
+//               table, and this CTA's rows of the shared expert straight into
+//               registers.  After it: the top-k of the logits (all warps),
+//               then this CTA's share of the routed experts' gate/up row
+//               pairs, loaded straight into registers (every load in flight
+//               at once, so the dot products run as the bytes arrive), and
+//               an L2 prefetch of the W_d rows the down kernel's CTA with the
+//               same index will read.  Each warp computes
+//                 a = silu(W_g x) * (W_u x)
+//               for its row pairs and writes a in fp32 (kRep copies).
+//   down_tok    one CTA of 256 threads per SM.  Before the wait: the same
+//               top-k.  After it: bulk copies of output rows [h0, h1) of
+//               every active expert's W_d (L2-warm), the fixed-point records
+//               of a, then
+//                 y[h] = sum_r w_r (W_d,r a_r)[h] + sigmoid(s) (W_d,sh a_sh)[h]
+//               for h in [h0, h1), summed in a fixed order.
 //
 // Dot products (the affine int4 format of MLX group quantisation, named on
 // the Swiftlet project page, "Relation to TurboFieldfare"): with
@@ -45,15 +51,19 @@
 namespace moe {
 namespace tok {
 
-constexpr int kMaxAct = 17;                          // top_k <= 16 plus the shared expert
-constexpr int kMaxE = 1024;                          // experts the staged tables hold
-constexpr uint64_t kWaitNs = 200ull * 1000 * 1000;   // 0.2 s bound on any barrier wait
-constexpr int kRec = 80;                             // bytes per fixed-point chunk record
-constexpr int kExThreads = 512;
-constexpr int kMaxSeg = 2;                           // gate/up segments per CTA
-constexpr int kMaxUnits = 8;                         // gate/up units (8 row pairs) per CTA
-constexpr int kParts = 1;                            // row parts per segment, one barrier each
-constexpr int kRowsPerWarp = 4;                      // gate/up row pairs per warp
+constexpr int kMaxAct = 17;    // top_k <= 16 plus the shared expert
+constexpr int kMaxE = 512;     // experts the single-token kernels take
+constexpr int kRec = 80;       // bytes per fixed-point chunk record
+constexpr int kGuWarps = 16;
+constexpr int kGuThreads = 32 * kGuWarps;
+constexpr int kMaxUnits = 5;   // gate/up units (8 row pairs) a CTA stages: 6 copy lanes each
+constexpr int kDnThreads = 256;
+
+// Bound on every device wait (ns) and extra arrivals the down kernel's copy
+// barrier expects.  Both are test hooks (moe_debug_set_waits): the defaults
+// are 0.2 s and 0.
+__device__ unsigned long long g_wait_ns = 200ull * 1000 * 1000;
+__device__ int g_extra_arrivals = 0;
 
 // ------------------------------------------------------------ PTX helpers
 
@@ -78,6 +88,11 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
                  : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 // Global -> shared bulk copy completing on `bar`.  Both addresses 16-byte
 // aligned, bytes a positive multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
@@ -88,27 +103,11 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
                  : "memory");
 }
 
-// 16-byte global -> shared copy through L2 (cp.async); both addresses
-// 16-byte aligned.  Every thread issues its own pieces, so a CTA stages a
-// weight slice without the per-copy setup cost of a bulk copy.
-__device__ __forceinline__ void cp16(void *dst, const void *src)
+// Fire-and-forget bulk prefetch of global bytes into L2 (16-byte aligned
+// address, size a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
 {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
-
-// Arrive on `bar` once every cp.async this thread has issued so far has
-// landed (the barrier's count includes this arrival).
-__device__ __forceinline__ void cp_arrive(uint64_t *bar)
-{
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-// Copy `bytes` (a multiple of 16) cooperatively: thread t of nt takes the
-// 16-byte pieces t, t + nt, ...
-__device__ __forceinline__ void cp_slice(void *dst, const void *src, uint32_t bytes, int t, int nt)
-{
-    for (uint32_t o = (uint32_t)t * 16; o < bytes; o += (uint32_t)nt * 16)
-        cp16(static_cast<char *>(dst) + o, static_cast<const char *>(src) + o);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // One potentially blocking test of the barrier's phase: the thread sleeps
@@ -133,18 +132,17 @@ __device__ __forceinline__ uint64_t global_ns()
     return t;
 }
 
-// Wait for phase 0 of a single-use barrier for at most kWaitNs; false (with
-// MOE_ERR_TIMEOUT recorded) if it never completes.  Inlined: a call would
-// make the caller's loads still in flight land before it.
+// Wait for phase 0 of a single-use barrier for at most g_wait_ns; false (with
+// MOE_ERR_TIMEOUT recorded) if it does not complete in time.
 __device__ __forceinline__ bool mbar_wait0(uint64_t *bar)
 {
     if (mbar_try_wait(bar, 0))
         return true;
-    const uint64_t t0 = global_ns();
+    const uint64_t t0 = global_ns(), lim = g_wait_ns;
     for (;;) {
         if (mbar_try_wait(bar, 0))
             return true;
-        if (global_ns() - t0 > kWaitNs) {
+        if (global_ns() - t0 > lim) {
             record_error(MOE_ERR_TIMEOUT);
             return false;
         }
@@ -188,21 +186,6 @@ __device__ __forceinline__ Chunk load_chunk(const unsigned char *rec)
     c.ho = p[2];
     c.lo = p[3];
     const float2 f = *reinterpret_cast<const float2 *>(rec + 64);
-    c.sx = f.x;
-    c.X = f.y;
-    return c;
-}
-
-// The same from global memory through L2 (written by another CTA).
-__device__ __forceinline__ Chunk load_chunk_global(const unsigned char *rec)
-{
-    Chunk c;
-    const uint4 *p = reinterpret_cast<const uint4 *>(rec);
-    c.he = __ldcg(p);
-    c.le = __ldcg(p + 1);
-    c.ho = __ldcg(p + 2);
-    c.lo = __ldcg(p + 3);
-    const float2 f = __ldcg(reinterpret_cast<const float2 *>(rec + 64));
     c.sx = f.x;
     c.X = f.y;
     return c;
@@ -281,165 +264,157 @@ __device__ __forceinline__ float chunk_term(uint4 q, const Chunk &c, float s, fl
     return fmaf(s, D, b * c.X);
 }
 
-template <typename TS> __device__ __forceinline__ float ld_sb(const TS *p) { return to_f32(*p); }
-
 // ------------------------------------------------------------ top-k
 
-// Does (va, ea) rank before (vb, eb) under (logit descending, id ascending)?
-__device__ __forceinline__ bool ranks_before(float va, int ea, float vb, int eb)
+// 32-bit order key of a logit: unsigned order = float order, NaN as -inf;
+// every real key is nonzero.
+__device__ __forceinline__ uint32_t ord32(float f)
 {
-    return va > vb || (va == vb && ea < eb);
+    const uint32_t u = __float_as_uint(isnan(f) ? -INFINITY : f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
-
-// Routing keys: one 64-bit unsigned integer per logit whose order is the
-// routing order (logit descending, then expert id ascending): the logit's bits
-// mapped to an unsigned order in the high word (NaN as -inf), the complement
-// of the id in the low word.
-__device__ __forceinline__ unsigned long long route_key(float f, int e)
+__device__ __forceinline__ float ord32_logit(uint32_t u)
 {
-    uint32_t u = __float_as_uint(isnan(f) ? -INFINITY : f);
-    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-    return ((unsigned long long)u << 32) | (0xFFFFFFFFu - (uint32_t)e);
-}
-__device__ __forceinline__ float key_logit(unsigned long long key)
-{
-    uint32_t u = (uint32_t)(key >> 32);
     u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
     return __uint_as_float(u);
 }
-__device__ __forceinline__ int key_expert(unsigned long long key) { return (int)(0xFFFFFFFFu - (uint32_t)key); }
-
-// Shared scratch of one warp's top-k.
-struct TopkSmem {
-    unsigned long long lm[32];   // lane maxima
-    unsigned long long cand[32]; // candidates
-    unsigned long long sel[16];  // the top k in rank order
-};
-
-// Top-k of the E <= 32*PER logits at lg (global, written by an earlier
-// kernel) by one warp.  Fills s_idx[r] / s_w[r] for r < k with the r-th
-// expert and its renormalised weight exp(l_r - l_0) / sum_{j<k} exp(l_j - l_0)
-// (and idx_out / w_out when idx_out is non-NULL).
-//
-// Lane l holds the keys of experts l + 32 j in registers.  T = the k-th
-// largest of the 32 lane maxima: every member of the top k is >= T, since k
-// lane maxima are.  The candidates (keys >= T, usually about k of them) are
-// ranked by counting over shared-memory broadcast reads.  If a lane holds
-// more than two candidates, or there are more than 32, rounds of warp
-// arg-max pick the same list instead.
-template <int PER>
-__device__ __noinline__ void warp_topk(const float *lg, int E, int k, int lane, TopkSmem &S, int *s_idx,
-                                       float *s_w, int32_t *idx_out, float *w_out)
+// Routing key: the order key in the high word, the complement of the expert
+// id in the low word, so that the key order is the routing order (logit
+// descending, then expert id ascending).
+__device__ __forceinline__ unsigned long long route_key(uint32_t u, int e)
 {
-    unsigned long long kv[PER];
-#pragma unroll
-    for (int j = 0; j < PER; ++j) {
-        const int e = lane + 32 * j;
-        kv[j] = e < E ? route_key(__ldcg(lg + e), e) : 0ull;
-    }
-    unsigned long long m[PER];
-#pragma unroll
-    for (int j = 0; j < PER; ++j)
-        m[j] = kv[j];
-#pragma unroll
-    for (int w = PER / 2; w > 0; w >>= 1)
-#pragma unroll
-        for (int j = 0; j < w; ++j)
-            m[j] = max(m[j], m[j + w]);
-    S.lm[lane] = m[0];
-    __syncwarp();
-    int rank = 0;
-#pragma unroll
-    for (int o = 0; o < 32; o += 2) {
-        const ulonglong2 q = *reinterpret_cast<const ulonglong2 *>(&S.lm[o]);
-        rank += (q.x > m[0] ? 1 : 0) + (q.y > m[0] ? 1 : 0);
-    }
-    const unsigned long long T = S.lm[__ffs(__ballot_sync(0xFFFFFFFFu, rank == k - 1)) - 1];
-    int cnt = 0;
-    unsigned long long c1 = 0, c2 = 0;
-#pragma unroll
-    for (int j = 0; j < PER; ++j) {
-        const bool ge = kv[j] >= T;
-        c2 = (ge && cnt == 1) ? kv[j] : c2;
-        c1 = (ge && cnt == 0) ? kv[j] : c1;
-        cnt += ge ? 1 : 0;
-    }
-    const uint32_t b1 = __ballot_sync(0xFFFFFFFFu, cnt >= 1), b2 = __ballot_sync(0xFFFFFFFFu, cnt >= 2);
-    const bool many = __any_sync(0xFFFFFFFFu, cnt > 2);
-    const int C = __popc(b1) + __popc(b2);
-    if (!many && C <= 32) {
-        const uint32_t lt = (1u << lane) - 1u;
-        const int p1 = __popc(b1 & lt) + __popc(b2 & lt);
-        if (cnt >= 1)
-            S.cand[p1] = c1;
-        if (cnt >= 2)
-            S.cand[p1 + 1] = c2;
-        __syncwarp();
-        const unsigned long long cv = lane < C ? S.cand[lane] : 0ull;
-        int r = 0;
-        for (int o = 0; o < C; o += 2) {
-            const ulonglong2 q = *reinterpret_cast<const ulonglong2 *>(&S.cand[o]);
-            r += (q.x > cv ? 1 : 0) + ((o + 1 < C && q.y > cv) ? 1 : 0);
-        }
-        if (lane < C && r < k)
-            S.sel[r] = cv;
-    } else {
-        unsigned long long prev = ~0ull;
-        for (int r = 0; r < k; ++r) {
-            unsigned long long best = 0;
-#pragma unroll
-            for (int j = 0; j < PER; ++j)
-                best = (kv[j] < prev && kv[j] > best) ? kv[j] : best;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-                best = max(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
-            if (lane == 0)
-                S.sel[r] = best;
-            prev = best;
-        }
-    }
-    __syncwarp();
-    const float l0 = key_logit(S.sel[0]);
-    float sv = -INFINITY;
-    int se = 0;
-    if (lane < k) {
-        const unsigned long long q = S.sel[lane];
-        sv = key_logit(q);
-        se = key_expert(q);
-    }
-    const float ex = lane < k ? expf(sv - l0) : 0.f;
-    const float wv = ex / warp_sum(ex);
-    if (lane < k) {
-        s_idx[lane] = se;
-        s_w[lane] = wv;
-        if (idx_out) {
-            idx_out[lane] = se;
-            w_out[lane] = wv;
-        }
-    }
-    __syncwarp();
+    return ((unsigned long long)u << 32) | (0xFFFFFFFFu - (uint32_t)e);
 }
 
-// Routing of this token into s_idx / s_w (shared memory), from logits copy
-// `rep` or from the given idx / w.  Warp 0 only.
-__device__ __forceinline__ void load_routing(const Routing &R, int rep, int E, int k, int lane, int *s_idx,
-                                             float *s_w, TopkSmem &S, bool write_out)
+// Shared scratch of the block top-k.
+struct TopkBlk {
+    uint32_t gm[32];                   // group maxima
+    unsigned long long cand[kMaxE];    // candidates (routing keys)
+    unsigned long long sel[16];        // the top k in rank order
+    int wcnt[32];                      // candidates per warp
+};
+
+// Top k of the E <= EPT NT logits at lg (global memory, written by an earlier
+// kernel) by all threads of the CTA; thread t < NT holds experts t + NT j
+// (NT a power of two, at least 32; threads past NT hold none).
+//
+// The keys are cut into 32 groups of NT / 32 consecutive threads.  T = the
+// group maximum of the largest rank <= k - 1 is at most the k-th largest key
+// (at least k keys are >= T), so the top k are among the candidates >= T,
+// usually about k of them.  Each warp ranks some candidates against all of
+// them, 32 at a time by ballot, comparing routing keys; a candidate's rank
+// among the candidates is its rank among all keys.
+//
+// Writes s_idx[r] (r < k), the r-th expert; when s_w is non-NULL also its
+// renormalised weight exp(l_r - l_0) / sum_{j<k} exp(l_j - l_0) to s_w[r],
+// and, when idx_out is non-NULL, both to idx_out / w_out.  Ends synchronised.
+template <int NT, int EPT>
+__device__ __forceinline__ void block_topk(const float *lg, int E, int k, TopkBlk &S, int *s_idx, float *s_w,
+                                           int32_t *idx_out, float *w_out)
+{
+    constexpr int GS = NT / 32;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5, nw = blockDim.x >> 5;
+    uint32_t u[EPT], m = 0;
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) {
+        const int e = t + NT * j;
+        u[j] = (t < NT && e < E) ? ord32(__ldcg(lg + e)) : 0u;
+        m = max(m, u[j]);
+    }
+#pragma unroll
+    for (int o = GS / 2; o > 0; o >>= 1)
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (t < NT && t % GS == 0)
+        S.gm[t / GS] = m;
+    __syncthreads();
+    const uint32_t g = S.gm[lane];
+    int r = 0;
+#pragma unroll
+    for (int o = 0; o < 32; o += 4) {
+        const uint4 q = *reinterpret_cast<const uint4 *>(&S.gm[o]);
+        r += (q.x > g ? 1 : 0) + (q.y > g ? 1 : 0) + (q.z > g ? 1 : 0) + (q.w > g ? 1 : 0);
+    }
+    const unsigned rmax = __reduce_max_sync(0xFFFFFFFFu, r <= k - 1 ? (unsigned)r : 0u);
+    const uint32_t T = __shfl_sync(0xFFFFFFFFu, g, __ffs(__ballot_sync(0xFFFFFFFFu, (unsigned)r == rmax)) - 1);
+    // candidates: counted per warp, then stored at the warp's offset
+    uint32_t bal[EPT];
+    int wn = 0;
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) {
+        bal[j] = __ballot_sync(0xFFFFFFFFu, u[j] != 0u && u[j] >= T);
+        wn += __popc(bal[j]);
+    }
+    if (lane == 0)
+        S.wcnt[warp] = wn;
+    __syncthreads();
+    const int before = (int)__reduce_add_sync(0xFFFFFFFFu, lane < warp && lane < nw ? (unsigned)S.wcnt[lane] : 0u);
+    const int C = (int)__reduce_add_sync(0xFFFFFFFFu, lane < nw ? (unsigned)S.wcnt[lane] : 0u);
+    int pos = before;
+    const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) {
+        if ((bal[j] >> lane) & 1u)
+            S.cand[pos + __popc(bal[j] & lt)] = route_key(u[j], t + NT * j);
+        pos += __popc(bal[j]);
+    }
+    __syncthreads();
+    for (int i = warp; i < C; i += nw) {
+        const unsigned long long ki = S.cand[i];
+        int rk = 0;
+        for (int b0 = 0; b0 < C; b0 += 32) {
+            const unsigned long long v = b0 + lane < C ? S.cand[b0 + lane] : 0ull;
+            rk += __popc(__ballot_sync(0xFFFFFFFFu, v > ki));
+        }
+        if (lane == 0 && rk < k)
+            S.sel[rk] = ki;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const unsigned long long q = lane < k ? S.sel[lane] : 0ull;
+        const int se = (int)(0xFFFFFFFFu - (uint32_t)q);
+        if (lane < k)
+            s_idx[lane] = se;
+        if (s_w) {
+            const float l0 = ord32_logit((uint32_t)(S.sel[0] >> 32));
+            const float ex = lane < k ? expf(ord32_logit((uint32_t)(q >> 32)) - l0) : 0.f;
+            float sum = ex;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+            const float wv = ex / sum;
+            if (lane < k) {
+                s_w[lane] = wv;
+                if (idx_out) {
+                    idx_out[lane] = se;
+                    w_out[lane] = wv;
+                }
+            }
+        }
+    }
+    __syncthreads();
+}
+
+// Routing of this token into s_idx (and s_w when non-NULL), shared memory:
+// the top-k of logits copy `rep`, or the given idx / w.  All threads; ends
+// synchronised.
+template <int NT>
+__device__ __forceinline__ void load_routing(const Routing &R, int rep, int E, int k, TopkBlk &S, int *s_idx,
+                                             float *s_w, bool write_out)
 {
     if (R.logits) {
         const float *lg = R.logits + (size_t)rep * R.lgs;
         int32_t *io = write_out ? R.idx_out : nullptr;
-        if (E <= 256)
-            warp_topk<8>(lg, E, k, lane, S, s_idx, s_w, io, R.w_out);
-        else if (E <= 512)
-            warp_topk<16>(lg, E, k, lane, S, s_idx, s_w, io, R.w_out);
+        if (E <= NT)
+            block_topk<NT, 1>(lg, E, k, S, s_idx, s_w, io, R.w_out);
         else
-            warp_topk<32>(lg, E, k, lane, S, s_idx, s_w, io, R.w_out);
+            block_topk<NT, kMaxE / NT>(lg, E, k, S, s_idx, s_w, io, R.w_out);
     } else {
-        if (lane < k) {
-            s_idx[lane] = __ldcg(R.idx + lane);
-            s_w[lane] = __ldcg(R.w + lane);
+        if ((int)threadIdx.x < k) {
+            s_idx[threadIdx.x] = __ldcg(R.idx + threadIdx.x);
+            if (s_w)
+                s_w[threadIdx.x] = __ldcg(R.w + threadIdx.x);
         }
-        __syncwarp();
+        __syncthreads();
     }
 }
 
@@ -470,17 +445,10 @@ __global__ void __launch_bounds__(128) router_tok_kernel(const __nv_bfloat16 *__
                                                         const __nv_bfloat16 *__restrict__ wsg,
                                                         float *__restrict__ lg, int lgs, int nrep,
                                                         float *__restrict__ sg, unsigned char *__restrict__ xrec,
-                                                        size_t xrs, unsigned int *__restrict__ bar, int n_row_ctas)
+                                                        size_t xrs, int n_row_ctas)
 {
     constexpr int H = 256 * NJ;
     pdl_trigger();
-    // the experts kernel that follows counts its CTAs through its grid
-    // barrier from zero (every kernel before this one has completed once the
-    // wait returns, so none still uses the counter)
-    if (bar && blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) {
-        pdl_wait();
-        *bar = 0u;
-    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if ((int)blockIdx.x >= n_row_ctas) {
         // fixed-point records of x: warp v converts chunks 4v .. 4v+3
@@ -520,7 +488,10 @@ __global__ void __launch_bounds__(128) router_tok_kernel(const __nv_bfloat16 *__
             acc1 = fmaf(__uint_as_float(wa[m] & 0xFFFF0000u), __uint_as_float(xa[m] & 0xFFFF0000u), acc1);
         }
     }
-    const float acc = warp_sum(acc0 + acc1);
+    float acc = acc0 + acc1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
     if (lane < nrep) {
         if (row < E)
             lg[(size_t)lane * lgs + row] = acc + (bias ? bias[row] : 0.f);
@@ -531,45 +502,28 @@ __global__ void __launch_bounds__(128) router_tok_kernel(const __nv_bfloat16 *__
         *sg = acc;
 }
 
-// ------------------------------------------------------------ experts
+// ------------------------------------------------------------ gate/up
 
-// One kernel computes the experts of the token: gate/up SwiGLU, then (after a
-// grid-wide barrier) down + weighted combine.
-//
-// Gate/up work comes in units of 8 row pairs (gate row o and up row o for 8
-// consecutive o), listed as [shared expert's units | rank 0's units | ...];
-// CTA c takes the contiguous run [c NU / n, (c + 1) NU / n), at most two
-// segments of consecutive rows of one expert.  It computes a = silu(g) u for
-// those rows and writes each unit's part of the fixed-point record of a (see
-// ARec).  After the barrier every CTA computes output rows [h0, h1) of y from
-// its rows of every active expert's W_d, one thread per 32-column chunk of a
-// (and half of the rows).
-//
-// Every code byte the CTA needs is bulk-copied into shared memory right after
-// the routing is known (each segment's gate and up code rows, and its rows of
-// each active expert's W_d), together with plain loads of the scale and bias
-// rows.  Latency-critical reads are kept out of that stream: small reads
-// issued while it is in flight wait behind it.
-struct ExpertsArgs {
+struct TokArgs {
     const unsigned char *xrec; // [kRep][xrs] fixed-point records of x
     size_t xrs;
     ExpertSrc src;
     Routing R;
-    unsigned char *arec;       // [kRep][ars]: ARec of each 32-row chunk of a
+    unsigned char *arec;       // [kRep][ars] activation records, one per 32-row chunk
     size_t ars;
-    unsigned int *bar;         // grid barrier counter, zeroed by the router kernel
     __nv_bfloat16 *y;
     float *y32;
     int E, k, I, Is, log2G;
 };
 
-// Fixed-point record of 32 consecutive values of a, written a quarter (8
-// values) at a time: for quarter m, he[m] le[m] ho[m] lo[m] hold the dp4a
-// bytes of its even and odd columns (as in Chunk), sx[m] its step and X[m]
-// its sum.  Quarter m occupies bytes 4m of each 16-byte field.
+// Activation record of one 32-row chunk of a, written 8 rows (a quarter) at
+// a time: for quarter m, he[m] le[m] ho[m] lo[m] hold the dp4a bytes of its
+// even and odd rows (as in Chunk), sx[m] its step and X[m] its sum.  Quarter
+// m occupies bytes 4m of each 16-byte field: he, le, ho, lo, sx[4], X[4].
 constexpr int kArec = 96;
 
-// Active expert *i of gate/up unit u of the list, and its first row *o0.
+// Gate/up unit u of the list [shared expert's units | rank 0's | rank 1's
+// ...] (8 row pairs each): active expert *i (k: the shared one), first row *o0.
 __device__ __forceinline__ void unit_of(int u, int k, int I, int Is, int *i, int *o0)
 {
     const int ns = Is >> 3;
@@ -589,15 +543,196 @@ __device__ __forceinline__ int chunk_index(int i, int ch, int k, int I, int Is)
     return i == k ? ch : (Is >> 5) + i * (I >> 5) + ch;
 }
 
-__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int *p)
+__device__ __forceinline__ void named_sync(int id, int nthreads)
 {
-    unsigned int v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// s * sum_c q_c a_c + b * sum_c a_c for one 32-code chunk of a W_d row and the
-// ARec fields he..lo (uint4 each, word m = quarter m), sx, X (float4).
+// H = 1024 * NXC; TS = scale/bias type.  One CTA of kGuThreads per SM.
+//
+// CTA c takes units [c NU / n, (c + 1) NU / n) of the unit list (NU units in
+// all).  Each unit is staged in shared memory by six bulk copies (its gate
+// and up code rows, its gate/up scale and bias rows) completing on the
+// unit's own barrier.  A CTA's shared-expert units are issued before the
+// wait; its routed units after the top-k, at most kDepth in flight: the
+// group that finds routed unit r landed issues unit r + kDepth, so the units
+// land one after another while the groups work on the earlier ones.  Warp
+// group g (warps 4g .. 4g + 3) computes units g, g + 4, ...: each warp two
+// row pairs of the unit, lane l taking chunks l and l + 32 of the row; then
+// lanes 0..7 of the group's first warp write the unit's quarter of its
+// chunk's activation record, one copy each.
+//
+// 80 registers a thread: with the down kernel (256 x 64) and the router (128
+// x 56) beside it, each of the SM's four register banks holds its share of
+// all three kernels, so each kernel's CTAs are resident before its
+// predecessor ends.
+template <int NXC, typename TS>
+__global__ void __maxnreg__(80) gateup_tok_kernel(TokArgs A)
+{
+    constexpr int H = 1024 * NXC;
+    constexpr int NG = kGuWarps / 4; // warp groups
+    constexpr int kDepth = 3;        // routed units in flight
+    extern __shared__ __align__(128) unsigned char units[]; // [local unit][unitb]
+    __shared__ uint64_t ubar[kMaxUnits], xbar;
+    __shared__ int tab[kMaxE];
+    __shared__ __align__(16) unsigned char xs[(H / 32) * kRec];
+    __shared__ __align__(16) TopkBlk tks;
+    __shared__ int s_idx[kMaxAct];
+    __shared__ const char *s_base[kMaxAct]; // blob of active expert i (i == k: shared), or nullptr
+    __shared__ float s_a[kMaxUnits][8];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n = gridDim.x, c = blockIdx.x, rep = c % kRep;
+    const int k = A.k;
+    const int NU = (A.Is >> 3) + k * (A.I >> 3);
+    const int u0 = (int)((long)c * NU / n), nu = (int)((long)(c + 1) * NU / n) - u0;
+    const int js = max(0, min(nu, (A.Is >> 3) - u0)); // local units [0, js) are the shared expert's
+    const int HG = H >> A.log2G;
+    const uint32_t sbr = (uint32_t)HG * (uint32_t)sizeof(TS); // bytes of one scale row
+    const uint32_t unitb = 8u * ((uint32_t)H + 4u * sbr);
+
+    // The copies of local unit j, by one warp: lane a < 6 copies array a
+    // (gate codes, up codes, gate scales, gate biases, up scales, up biases)
+    // of the unit's 8 rows; lane 0 arms the unit's barrier.
+    auto stage = [&](int j) {
+        int i, o0;
+        unit_of(u0 + j, k, A.I, A.Is, &i, &o0);
+        const char *b = s_base[i];
+        if (lane == 0)
+            mbar_expect_tx(&ubar[j], b ? unitb : 0u);
+        __syncwarp();
+        if (b && lane < 6) {
+            const size_t *offs = i == k ? A.src.off_sh : A.src.off;
+            unsigned char *d = units + (size_t)j * unitb;
+            if (lane < 2)
+                bulk_g2s(d + lane * 8 * (H / 2), b + offs[lane ? M_QU : M_QG] + (size_t)o0 * (H / 2), 8u * (H / 2),
+                         &ubar[j]);
+            else
+                bulk_g2s(d + 8 * H + (lane - 2) * 8 * sbr, b + offs[M_SG + (lane - 2)] + (size_t)o0 * sbr, 8u * sbr,
+                         &ubar[j]);
+        }
+    };
+
+    // ---- before the wait: barriers, the slot table, the shared expert's units
+    if (threadIdx.x == 0) {
+        for (int j = 0; j < nu; ++j)
+            mbar_init(&ubar[j], 1);
+        mbar_init(&xbar, 1);
+        fence_mbar_init();
+        s_base[k] = A.src.shared;
+    }
+    for (int e = threadIdx.x; e < A.E; e += kGuThreads)
+        tab[e] = __ldg(A.src.table + e);
+    __syncthreads();
+    if (warp == kGuWarps - 1)
+        for (int j = 0; j < js; ++j)
+            stage(j);
+
+    pdl_wait();
+    pdl_trigger(); // the router has completed: the down kernel may start its own top-k
+
+    // ---- x's records, the routing, the first routed units
+    if (threadIdx.x == 0) {
+        constexpr uint32_t xb = (H / 32) * kRec;
+        mbar_expect_tx(&xbar, xb);
+        bulk_g2s(xs, A.xrec + (size_t)rep * A.xrs, xb, &xbar);
+    }
+    load_routing<kGuThreads>(A.R, rep, A.E, k, tks, s_idx, nullptr, false);
+    if ((int)threadIdx.x < k)
+        s_base[threadIdx.x] = routed_base(A.src, tab, s_idx[threadIdx.x]);
+    __syncthreads();
+    if (warp == kGuWarps - 1)
+        for (int j = js; j < min(nu, js + kDepth); ++j)
+            stage(j);
+
+    // ---- gate/up: this lane's chunks of x, then the group's units
+    const bool xok = __all_sync(0xFFFFFFFFu, mbar_wait0(&xbar));
+    Chunk xv[NXC];
+#pragma unroll
+    for (int m = 0; m < NXC; ++m)
+        xv[m] = load_chunk(xs + (size_t)(lane + 32 * m) * kRec);
+    const int grp = warp >> 2, wq = warp & 3;
+    for (int j = grp; j < nu; j += NG) {
+        int i, o0;
+        unit_of(u0 + j, k, A.I, A.Is, &i, &o0);
+        const bool have = xok && s_base[i] != nullptr && __all_sync(0xFFFFFFFFu, mbar_wait0(&ubar[j]));
+        if (wq == 0 && j >= js && j + kDepth < nu)
+            stage(j + kDepth);
+        const unsigned char *d = units + (size_t)j * unitb;
+        const TS *sc = reinterpret_cast<const TS *>(d + 8 * H);
+        float v[4] = {0.f, 0.f, 0.f, 0.f}; // gate, up of rows 2 wq and 2 wq + 1
+        if (have) {
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int r = 2 * wq + rr;
+#pragma unroll
+                for (int m = 0; m < NXC; ++m) {
+                    const int ch = lane + 32 * m;
+                    const int gi = (ch * 32) >> A.log2G;
+                    const uint4 qg = reinterpret_cast<const uint4 *>(d + r * (H / 2))[ch];
+                    const uint4 qu = reinterpret_cast<const uint4 *>(d + 8 * (H / 2) + r * (H / 2))[ch];
+                    v[2 * rr] += chunk_term(qg, xv[m], to_f32(sc[r * HG + gi]), to_f32(sc[8 * HG + r * HG + gi]));
+                    v[2 * rr + 1] +=
+                        chunk_term(qu, xv[m], to_f32(sc[16 * HG + r * HG + gi]), to_f32(sc[24 * HG + r * HG + gi]));
+                }
+            }
+        }
+        // transposing reduction of the four sums: lanes with bit 4 set keep
+        // values 2, 3, the others 0, 1; then bit 3 splits those
+        {
+            const bool hi = (lane & 16) != 0;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const float send = hi ? v[q] : v[q + 2];
+                const float keep = hi ? v[q + 2] : v[q];
+                v[q] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+            }
+            const bool h8 = (lane & 8) != 0;
+            const float send = h8 ? v[0] : v[1];
+            const float keep = h8 ? v[1] : v[0];
+            v[0] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
+#pragma unroll
+            for (int o = 4; o > 0; o >>= 1)
+                v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], o);
+        }
+        // lane l holds value 2 (l >> 4) + ((l >> 3) & 1): gate or up of row 2 wq + (l >> 4)
+        const float up = __shfl_xor_sync(0xFFFFFFFFu, v[0], 8);
+        if ((lane & 15) == 0)
+            s_a[j][2 * wq + (lane >> 4)] = have ? v[0] * sigmoid_f(v[0]) * up : 0.f;
+        named_sync(1 + grp, 128);
+        if (wq == 0 && lane < kRep) {
+            float a[8], am = 0.f, X = 0.f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                a[q] = s_a[j][q];
+                am = fmaxf(am, fabsf(a[q]));
+                X += a[q];
+            }
+            const bool nz = am > 0.f && am < INFINITY;
+            const float inv = nz ? 32767.0f / am : 0.f;
+            uint32_t f[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                f[q] = __float_as_uint(fmaf(a[q], inv, 12582912.0f));
+            // byte q of he / le: rows 2q (high / low byte); of ho / lo: 2q + 1
+            const uint32_t e01 = __byte_perm(f[0], f[2], 0x5140), e23 = __byte_perm(f[4], f[6], 0x5140);
+            const uint32_t o01 = __byte_perm(f[1], f[3], 0x5140), o23 = __byte_perm(f[5], f[7], 0x5140);
+            const int mq = (o0 & 31) >> 3;
+            unsigned char *rec = A.arec + (size_t)lane * A.ars + (size_t)chunk_index(i, o0 >> 5, k, A.I, A.Is) * kArec + 4 * mq;
+            *reinterpret_cast<uint32_t *>(rec) = __byte_perm(e01, e23, 0x7632);
+            *reinterpret_cast<uint32_t *>(rec + 16) = __byte_perm(e01, e23, 0x5410);
+            *reinterpret_cast<uint32_t *>(rec + 32) = __byte_perm(o01, o23, 0x7632);
+            *reinterpret_cast<uint32_t *>(rec + 48) = __byte_perm(o01, o23, 0x5410);
+            *reinterpret_cast<float *>(rec + 64) = nz ? am / 32767.0f : 0.f;
+            *reinterpret_cast<float *>(rec + 80) = X;
+        }
+    }
+}
+
+// ------------------------------------------------------------ down
+
+// s * sum_c q_c a_c + b * sum_c a_c for one 32-code chunk of a W_d row and an
+// activation record's fields he..lo (uint4 each, word m = quarter m), sx, X.
 __device__ __forceinline__ float arec_term(uint4 q, uint4 he, uint4 le, uint4 ho, uint4 lo, float4 sx, float4 X,
                                            float s, float b)
 {
@@ -617,359 +752,145 @@ __device__ __forceinline__ float arec_term(uint4 q, uint4 he, uint4 le, uint4 ho
     return fmaf(s, D, b * ((X.x + X.y) + (X.z + X.w)));
 }
 
-// H = 1024 * NXC; TS = scale/bias type.  One CTA of kExThreads per SM.
-//
-// Shared memory (dynamic): per segment [n gate code rows][n up code rows]
-// [n gate scale rows][n gate bias rows][n up scale rows][n up bias rows];
-// then per active expert its down rows (codes [nr][I_i/2], scales and biases
-// [nr][I_i/G] each); then the partial sums of the down phase.
-template <int NXC, typename TS>
-__global__ void __maxnreg__(112) experts_tok_kernel(ExpertsArgs A)
+// Down projection and combine.  CTA c computes output rows [h0, h1) =
+// [c H / n, (c + 1) H / n).  Its W_d rows of every active expert (codes
+// [nr][I_i/2], then scales and biases [nr][I_i/G] each, per expert; L2-warm
+// from the gate/up kernel's prefetch) and the activation records are bulk-
+// copied into shared memory; thread t owns chunks t, t + kDnThreads, ... of
+// the chunk list [shared | rank 0 | rank 1 | ...]: it writes w_i times its
+// chunk's term of each output row to P[row][chunk].  Warps then sum each row
+// over the chunks in a fixed order, so the result does not depend on where
+// the experts live.  The routing (with weights) is computed before the wait.
+template <typename TS>
+__global__ void __maxnreg__(64) down_tok_kernel(TokArgs A, int H)
 {
-    constexpr int H = 1024 * NXC;
-    constexpr int NW = kExThreads / 32;
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ uint64_t sbar[kMaxSeg][kParts], dbar, xbar;
+    __shared__ uint64_t dbar, rbar;
     __shared__ int tab[kMaxE];
-    __shared__ __align__(16) unsigned char xs[(H / 32) * kRec];
+    __shared__ __align__(16) TopkBlk tks;
     __shared__ int s_idx[kMaxAct];
     __shared__ float s_w[kMaxAct + 1];
-    __shared__ const char *s_base[kMaxAct];  // blob of active expert i (i == k: shared), or nullptr
-    __shared__ uint32_t s_eoff[kMaxAct + 1]; // offset of expert i's down rows in the down region
-    __shared__ int s_qb[kMaxAct];            // down code bytes per row of expert i
-    __shared__ int s_ng[kMaxAct];            // down groups per row of expert i
-    __shared__ float s_a[8 * kMaxUnits];
-    __shared__ __align__(16) TopkSmem tks;
+    __shared__ const char *s_base[kMaxAct];
+    __shared__ uint32_t s_eoff[kMaxAct + 1]; // offset of expert i's rows in the down region
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int n = gridDim.x, c = blockIdx.x, rep = c % kRep;
     const int k = A.k, n_act = k + 1;
-    const int HG = H >> A.log2G;                     // groups per gate/up row
-    const uint32_t qrow = H / 2;                     // code bytes per gate/up row
-    const uint32_t sb = sizeof(TS);
-    const uint32_t srow = (uint32_t)HG * sb;         // scale (or bias) bytes per gate/up row
-    const uint32_t rowb = 2 * qrow + 4 * srow;       // shared bytes per row pair of a segment
-    const int NU = (A.Is >> 3) + k * (A.I >> 3);
+    const int h0 = (int)((long)c * H / n), nr = (int)((long)(c + 1) * H / n) - h0;
     const int NC = (A.Is >> 5) + k * (A.I >> 5);
-    const int u0 = (int)((long)c * NU / n), u1 = (int)((long)(c + 1) * NU / n);
-    // segments: runs of this CTA's units within one expert
-    int nseg = 0, seg_i[kMaxSeg], seg_o0[kMaxSeg], seg_n[kMaxSeg];
-    uint32_t seg_off[kMaxSeg];
-    {
-        uint32_t off = 0;
-        for (int u = u0; u < u1 && nseg < kMaxSeg;) {
-            int i, o0;
-            unit_of(u, k, A.I, A.Is, &i, &o0);
-            const int inter = (i == k) ? A.Is : A.I;
-            const int len = min(u1 - u, (inter - o0) >> 3);
-            seg_i[nseg] = i;
-            seg_o0[nseg] = o0;
-            seg_n[nseg] = 8 * len;
-            seg_off[nseg] = off;
-            off += (uint32_t)(8 * len) * rowb;
-            ++nseg;
-            u += len;
-        }
-    }
-    const int NR = 8 * (u1 - u0); // row pairs of this CTA
-    unsigned char *down = smem + (nseg ? seg_off[nseg - 1] + (uint32_t)seg_n[nseg - 1] * rowb : 0u);
-    const int h0 = (int)((long)c * (long)H / n), h1 = (int)((long)(c + 1) * (long)H / n);
-    const int nr = h1 - h0;
+    const uint32_t sb = sizeof(TS);
 
-    // The copy warp (the last one; it computes no gate/up rows, since a bulk
-    // copy holds its issuing thread until the copy engine takes it) stages
-    // part p of segment s (rows [r0, r1) = [p n / kParts, (p + 1) n / kParts))
-    // with lanes 6 (s kParts + p) + j: j < 4 copies those rows of the gate
-    // scales, gate biases, up scales, up biases (small, so issued first),
-    // j = 4 / 5 the gate / up code rows; lane j = 0 arms the part's barrier.
-    // Only segments with `pick` set.
-    auto stage_rows = [&](bool (*pick)(int, int), const char *const *base) {
-        const int q = lane / 6, j = lane - 6 * q, s = q / kParts, p = q - s * kParts;
-        const bool valid = q < kMaxSeg * kParts && s < nseg && pick(seg_i[s], k);
-        const bool on = valid && base[s] != nullptr;
-        uint32_t r0 = 0, nrow = 0;
-        if (valid) {
-            r0 = (uint32_t)(p * seg_n[s] / kParts);
-            nrow = (uint32_t)((p + 1) * seg_n[s] / kParts) - r0;
-        }
-        if (valid && j == 0 && nrow)
-            mbar_expect_tx(&sbar[s][p], on ? nrow * rowb : 0u);
-        __syncwarp();
-        if (on && nrow) {
-            const size_t *offs = (seg_i[s] == k) ? A.src.off_sh : A.src.off;
-            const uint32_t nn = (uint32_t)seg_n[s];
-            unsigned char *d = smem + seg_off[s];
-            const size_t row = (size_t)(seg_o0[s] + (int)r0);
-            if (j < 4) {
-                const int m = j == 0 ? M_SG : j == 1 ? M_BG : j == 2 ? M_SU : M_BU;
-                bulk_g2s(d + 2 * nn * qrow + j * nn * srow + r0 * srow, base[s] + offs[m] + row * srow, nrow * srow,
-                         &sbar[s][p]);
-            } else {
-                const int h = j - 4;
-                bulk_g2s(d + h * nn * qrow + r0 * qrow, base[s] + offs[h ? M_QU : M_QG] + row * qrow, nrow * qrow,
-                         &sbar[s][p]);
-            }
-        }
-    };
-
-    // ---- before the wait: only what does not depend on the router's output
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kMaxSeg; ++s)
-            for (int p = 0; p < kParts; ++p)
-                mbar_init(&sbar[s][p], 1);
-        mbar_init(&dbar, 1);
-        mbar_init(&xbar, kExThreads);
+    // ---- before the wait: slot table, routing, region offsets
+    if (t == 0) {
+        mbar_init(&dbar, 1u + (uint32_t)g_extra_arrivals);
+        mbar_init(&rbar, 1);
         fence_mbar_init();
-        uint32_t o = 0;
+        uint32_t off = 0;
         for (int i = 0; i < n_act; ++i) {
-            const int inter = (i == k) ? A.Is : A.I;
-            s_eoff[i] = o;
-            s_qb[i] = inter / 2;
-            s_ng[i] = inter >> A.log2G;
-            o += (uint32_t)nr * ((uint32_t)inter / 2 + 2 * (uint32_t)(inter >> A.log2G) * sb);
+            const int inter = i == k ? A.Is : A.I;
+            s_eoff[i] = off;
+            off += (uint32_t)nr * ((uint32_t)inter / 2 + 2 * (uint32_t)(inter >> A.log2G) * sb);
         }
-        s_eoff[n_act] = o;
+        s_eoff[n_act] = off;
         s_base[k] = A.src.shared;
     }
-    for (int e = threadIdx.x; e < A.E; e += kExThreads)
+    for (int e = t; e < A.E; e += kDnThreads)
         tab[e] = __ldg(A.src.table + e);
-    __syncthreads();
-    // the shared expert's units come first in the list: stage them now
-    if (warp == NW - 1) {
-        const char *base[kMaxSeg] = {A.src.shared, A.src.shared};
-        stage_rows([](int i, int kk) { return i == kk; }, base);
-    }
-
-    // ---- after the wait: x records and the shared-gate logit are fetched
-    // while warp 0 selects the top k; then every copy is issued
-    pdl_wait();
-    cp_slice(xs, A.xrec + (size_t)rep * A.xrs, (H / 32) * kRec, threadIdx.x, kExThreads);
-    cp_arrive(&xbar);
-    if (threadIdx.x == 32)
+    load_routing<kDnThreads>(A.R, rep, A.E, k, tks, s_idx, s_w, false);
+    if (t < k)
+        s_base[t] = routed_base(A.src, tab, s_idx[t]);
+    if (t == 32)
         s_w[kMaxAct] = sigmoid_f(__ldcg(A.R.logits ? A.R.logits + (size_t)rep * A.R.lgs + A.E : A.R.sg_logit));
-    if (warp == 0) {
-        load_routing(A.R, rep, A.E, k, lane, s_idx, s_w, tks, c == 0);
-        if (lane < k)
-            s_base[lane] = routed_base(A.src, tab, s_idx[lane]);
-    }
     __syncthreads();
-    // the copy warp: routed gate/up rows; then, once every gate/up part of
-    // this SM has landed (the down rows are needed only after the grid
-    // barrier, so they must not compete with the gate/up stream), lane 12 + i
-    // copies expert i's down code, scale and bias rows [h0, h1) (lane 12 arms
-    // the barrier)
-    if (warp == NW - 1) {
-        const char *base[kMaxSeg];
-        for (int s = 0; s < kMaxSeg; ++s)
-            base[s] = s < nseg ? s_base[seg_i[s]] : nullptr;
-        stage_rows([](int i, int kk) { return i != kk; }, base);
-        for (int s = 0; s < nseg; ++s)
-            for (int p = 0; p < kParts; ++p)
-                if ((p + 1) * seg_n[s] / kParts > p * seg_n[s] / kParts)
-                    mbar_wait0(&sbar[s][p]);
-        const int i = lane - 12;
-        const char *b = (i >= 0 && i < n_act) ? s_base[i] : nullptr;
-        const uint32_t nq = b ? (uint32_t)nr * s_qb[i] : 0u, ns = b ? (uint32_t)(nr * s_ng[i]) * sb : 0u;
-        const uint32_t tot = __reduce_add_sync(0xFFFFFFFFu, nq + 2 * ns);
-        if (lane == 12)
+
+    // ---- the W_d rows [h0, h1) of every active expert (weights: not written
+    // by the kernels this one waits for, so copied before the wait)
+    unsigned char *down = smem;
+    unsigned char *rec = smem + ((s_eoff[n_act] + 127) & ~127u); // [NC][kArec]
+    float *P = reinterpret_cast<float *>(rec + (size_t)NC * kArec); // [nr][NC]
+    if (warp == 0) {
+        const char *b = lane < n_act ? s_base[lane] : nullptr;
+        const int inter = lane == k ? A.Is : A.I;
+        const uint32_t qb = (uint32_t)inter / 2, sbb = (uint32_t)(inter >> A.log2G) * sb;
+        const uint32_t nq = b ? (uint32_t)nr * qb : 0u, nsb = b ? (uint32_t)nr * sbb : 0u;
+        const uint32_t tot = __reduce_add_sync(0xFFFFFFFFu, nq + 2 * nsb);
+        if (lane == 0)
             mbar_expect_tx(&dbar, tot);
         __syncwarp();
         if (b && nq) {
-            const size_t *offs = (i == k) ? A.src.off_sh : A.src.off;
-            unsigned char *d = down + s_eoff[i];
-            bulk_g2s(d, b + offs[M_QD] + (size_t)h0 * s_qb[i], nq, &dbar);
-            bulk_g2s(d + nq, b + offs[M_SD] + (size_t)h0 * s_ng[i] * sb, ns, &dbar);
-            bulk_g2s(d + nq + ns, b + offs[M_BD] + (size_t)h0 * s_ng[i] * sb, ns, &dbar);
-        }
-    }
-    constexpr int NWC = NW - 1; // gate/up warps
-
-    // ---- gate/up: warp w < NWC computes row pairs w, w + NWC, ... (at most
-    // kRowsPerWarp).  Every row's dot products come first, with no wait
-    // between rows, so that their loads and dp4a chains overlap; then one
-    // transposing reduction sums all 2 kRowsPerWarp partial values across
-    // the warp (9 shuffles instead of 10 per row).
-    static_assert(kRowsPerWarp == 4 && kParts == 1, "the reduction below assumes 4 rows per warp, 1 part");
-    if (!__all_sync(0xFFFFFFFFu, mbar_wait0(&xbar)))
-        return;
-    // lane l owns chunks NXC l ... of a row; with two chunks, lanes 4-7 of
-    // each quarter warp take them in the other order (xv[m] is chunk
-    // 2 l + (m ^ sw)), which makes each 16-byte code load conflict-free
-    const int sw = NXC == 2 ? (lane >> 2) & 1 : 0;
-    Chunk xv[NXC];
-    float Xs = 0.f; // sum of this lane's x columns (its quantisation group)
-#pragma unroll
-    for (int m = 0; m < NXC; ++m) {
-        xv[m] = load_chunk(xs + (size_t)(NXC * lane + (m ^ sw)) * kRec);
-        Xs += xv[m].X;
-    }
-    bool landed = warp < NWC;
-    if (landed)
-        for (int s = 0; s < nseg; ++s)
-            landed &= mbar_wait0(&sbar[s][0]);
-    landed = __all_sync(0xFFFFFFFFu, landed);
-    float v[2 * kRowsPerWarp]; // gate, up partial sums of rows t = 0, 1, ...
-#pragma unroll
-    for (int t = 0; t < kRowsPerWarp; ++t) {
-        const int rp = warp + t * NWC;
-        float g = 0.f, u = 0.f;
-        if (landed && rp < NR) {
-            const int s = (nseg > 1 && rp >= seg_n[0]) ? 1 : 0, r = s ? rp - seg_n[0] : rp;
-            if (s_base[seg_i[s]]) {
-                const uint32_t nq = (uint32_t)seg_n[s] * qrow;
-                const unsigned char *d = smem + seg_off[s];
-                // this lane's group of row r: gate scale, gate bias, up scale, up bias
-                const TS *sc = reinterpret_cast<const TS *>(d + 2 * nq) + r * HG + ((NXC * lane * 32) >> A.log2G);
-                const int na = seg_n[s] * HG;
-                const uint4 *qg = reinterpret_cast<const uint4 *>(d + (size_t)r * qrow);
-                const uint4 *qu = reinterpret_cast<const uint4 *>(d + nq + (size_t)r * qrow);
-                // one quantisation group per lane: sum_m s (sx_m D_m) + b X_m
-                float Dg = 0.f, Du = 0.f;
-#pragma unroll
-                for (int m = 0; m < NXC; ++m) {
-                    Dg = fmaf((float)chunk_idot(qg[NXC * lane + (m ^ sw)], xv[m]), xv[m].sx, Dg);
-                    Du = fmaf((float)chunk_idot(qu[NXC * lane + (m ^ sw)], xv[m]), xv[m].sx, Du);
-                }
-                g = fmaf(to_f32(sc[0]), Dg, to_f32(sc[na]) * Xs);
-                u = fmaf(to_f32(sc[2 * na]), Du, to_f32(sc[3 * na]) * Xs);
-            }
-        }
-        v[2 * t] = g;
-        v[2 * t + 1] = u;
-    }
-    // round with half-count w: lanes with bit 4 w set keep values [w, 2 w),
-    // the others [0, w), each adding its partner's copy of the kept values
-#pragma unroll
-    for (int w = kRowsPerWarp; w >= 1; w >>= 1) {
-        const bool hi = (lane & (4 * w)) != 0;
-#pragma unroll
-        for (int j = 0; j < w; ++j) {
-            const float send = hi ? v[j] : v[j + w];
-            const float keep = hi ? v[j + w] : v[j];
-            v[j] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 4 * w);
-        }
-    }
-    v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], 2);
-    v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], 1);
-    // lane l now holds the total of value 2 t + h, t = (l >> 3) & 3, h = (l >> 2) & 1
-    const float up = __shfl_xor_sync(0xFFFFFFFFu, v[0], 4);
-    if ((lane & 7) == 0 && warp < NWC) {
-        const int rp = warp + (lane >> 3) * NWC;
-        if (rp < NR)
-            s_a[rp] = v[0] * sigmoid_f(v[0]) * up;
-    }
-    __syncthreads();
-    // each unit writes its quarter of a chunk's record, in kRep copies
-    if (threadIdx.x < u1 - u0) {
-        const int uu = u0 + threadIdx.x;
-        int i, o0;
-        unit_of(uu, k, A.I, A.Is, &i, &o0);
-        const float *v = s_a + 8 * threadIdx.x;
-        float am = 0.f, X = 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            am = fmaxf(am, fabsf(v[j]));
-            X += v[j];
-        }
-        const bool nz = am > 0.f && am < INFINITY;
-        const float inv = nz ? 32767.0f / am : 0.f;
-        uint32_t f[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            f[j] = __float_as_uint(fmaf(v[j], inv, 12582912.0f));
-        // byte j of he / le: columns 2j (high / low byte); of ho / lo: 2j + 1
-        const uint32_t e01 = __byte_perm(f[0], f[2], 0x5140), e23 = __byte_perm(f[4], f[6], 0x5140);
-        const uint32_t o01 = __byte_perm(f[1], f[3], 0x5140), o23 = __byte_perm(f[5], f[7], 0x5140);
-        const uint32_t he = __byte_perm(e01, e23, 0x7632), le = __byte_perm(e01, e23, 0x5410);
-        const uint32_t ho = __byte_perm(o01, o23, 0x7632), lo = __byte_perm(o01, o23, 0x5410);
-        const int m = (o0 & 31) >> 3;
-        unsigned char *rec = A.arec + (size_t)chunk_index(i, o0 >> 5, k, A.I, A.Is) * kArec + 4 * m;
-        const float sx = nz ? am / 32767.0f : 0.f;
-        for (int r = 0; r < kRep; ++r) {
-            unsigned char *rr = rec + (size_t)r * A.ars;
-            *reinterpret_cast<uint32_t *>(rr) = he;
-            *reinterpret_cast<uint32_t *>(rr + 16) = le;
-            *reinterpret_cast<uint32_t *>(rr + 32) = ho;
-            *reinterpret_cast<uint32_t *>(rr + 48) = lo;
-            *reinterpret_cast<float *>(rr + 64) = sx;
-            *reinterpret_cast<float *>(rr + 80) = X;
+            const size_t *offs = lane == k ? A.src.off_sh : A.src.off;
+            unsigned char *d = down + s_eoff[lane];
+            bulk_g2s(d, b + offs[M_QD] + (size_t)h0 * qb, nq, &dbar);
+            bulk_g2s(d + nq, b + offs[M_SD] + (size_t)h0 * sbb, nsb, &dbar);
+            bulk_g2s(d + nq + nsb, b + offs[M_BD] + (size_t)h0 * sbb, nsb, &dbar);
         }
     }
 
-    // ---- grid barrier: every record is written
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        atomicAdd(A.bar, 1u);
-        const uint64_t t0 = global_ns();
-        while (ld_acquire_u32(A.bar) < (unsigned int)n) {
-            if (global_ns() - t0 > kWaitNs) {
-                record_error(MOE_ERR_TIMEOUT);
-                break;
-            }
-        }
+    pdl_wait(); // the activation records are complete
+    pdl_trigger();
+    if (c == 0 && A.R.logits && A.R.idx_out && t < k) {
+        A.R.idx_out[t] = s_idx[t];
+        A.R.w_out[t] = s_w[t];
     }
-    __syncthreads();
-    pdl_trigger(); // the next layer call may start its own weight loads now
+    if (t == 0) {
+        const uint32_t rb = (uint32_t)NC * kArec;
+        mbar_expect_tx(&rbar, rb);
+        bulk_g2s(rec, A.arec + (size_t)rep * A.ars, rb, &rbar);
+    }
+    const bool rec_ok = mbar_wait0(&rbar);
+    bool ready = mbar_wait0(&dbar);
+    if (!ready && t == 0) {
+        // supply the arrivals a test asked for, then let the copies land
+        for (int j = 0; j < g_extra_arrivals; ++j)
+            mbar_arrive(&dbar);
+    }
+    if (!ready)
+        mbar_wait0(&dbar);
+    ready = __syncthreads_and(ready && rec_ok);
 
-    // ---- down, item by item: thread t < 2 NC owns chunk j = t % NC (chunk ch
-    // of active expert i; its record is loaded into registers) and half the
-    // CTA's output rows, [rg RH, rg RH + RH) with rg = t / NC.  It writes w_i
-    // times its part of each row to P[row][j]; warp w then sums row w over
-    // the chunks in a fixed order, so the result does not depend on where the
-    // experts live.
-    const int RH = (nr + 1) / 2;
-    float *P = reinterpret_cast<float *>(down + ((s_eoff[n_act] + 15) & ~15u)); // [nr][NC]
-    const int t = threadIdx.x;
-    const bool mine = t < 2 * NC;
-    const int j = mine ? t % NC : 0, rg = t / NC;
-    int ii, ch;
-    if (j < (A.Is >> 5)) {
-        ii = k;
-        ch = j;
-    } else {
-        ii = (j - (A.Is >> 5)) / (A.I >> 5);
-        ch = (j - (A.Is >> 5)) - ii * (A.I >> 5);
-    }
-    uint4 rv[6] = {};
-    if (mine) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(A.arec + (size_t)rep * A.ars + (size_t)j * kArec);
-#pragma unroll
-        for (int q = 0; q < 6; ++q)
-            rv[q] = __ldcg(src + q);
-    }
-    const bool ready = __all_sync(0xFFFFFFFFu, mbar_wait0(&dbar));
-    if (mine) {
-        const int r0 = rg * RH, r1 = min(nr, r0 + RH);
-        if (ready && s_base[ii]) {
-            const int qb = s_qb[ii], ng = s_ng[ii];
-            const unsigned char *d = down + s_eoff[ii];
-            const TS *sd = reinterpret_cast<const TS *>(d + nr * qb);
-            const TS *bd = sd + nr * ng;
-            const int g = (ch * 32) >> A.log2G;
-            const float wi = ii < k ? s_w[ii] : s_w[kMaxAct];
-            const float4 sx = make_float4(__uint_as_float(rv[4].x), __uint_as_float(rv[4].y),
-                                          __uint_as_float(rv[4].z), __uint_as_float(rv[4].w));
-            const float4 X = make_float4(__uint_as_float(rv[5].x), __uint_as_float(rv[5].y),
-                                         __uint_as_float(rv[5].z), __uint_as_float(rv[5].w));
-#pragma unroll 4
-            for (int r = r0; r < r1; ++r) {
-                const uint4 q = reinterpret_cast<const uint4 *>(d + r * qb)[ch];
-                P[r * NC + j] = wi * arec_term(q, rv[0], rv[1], rv[2], rv[3], sx, X, ld_sb(sd + r * ng + g),
-                                               ld_sb(bd + r * ng + g));
-            }
+    // ---- per-chunk terms of every output row
+    for (int j = t; j < NC; j += kDnThreads) {
+        int i, ch;
+        if (j < (A.Is >> 5)) {
+            i = k;
+            ch = j;
         } else {
-            for (int r = r0; r < r1; ++r)
+            i = (j - (A.Is >> 5)) / (A.I >> 5);
+            ch = (j - (A.Is >> 5)) - i * (A.I >> 5);
+        }
+        if (!ready || !s_base[i]) {
+            for (int r = 0; r < nr; ++r)
                 P[r * NC + j] = 0.f;
+            continue;
+        }
+        const uint4 *rv = reinterpret_cast<const uint4 *>(rec + (size_t)j * kArec);
+        const uint4 he = rv[0], le = rv[1], ho = rv[2], lo = rv[3], sxu = rv[4], Xu = rv[5];
+        const float4 sx = make_float4(__uint_as_float(sxu.x), __uint_as_float(sxu.y), __uint_as_float(sxu.z),
+                                      __uint_as_float(sxu.w));
+        const float4 X = make_float4(__uint_as_float(Xu.x), __uint_as_float(Xu.y), __uint_as_float(Xu.z),
+                                     __uint_as_float(Xu.w));
+        const int inter = i == k ? A.Is : A.I;
+        const int qb = inter / 2, ng = inter >> A.log2G;
+        const unsigned char *d = down + s_eoff[i];
+        const TS *sd = reinterpret_cast<const TS *>(d + nr * qb);
+        const TS *bd = sd + nr * ng;
+        const int g = (ch * 32) >> A.log2G;
+        const float wi = i < k ? s_w[i] : s_w[kMaxAct];
+#pragma unroll 4
+        for (int r = 0; r < nr; ++r) {
+            const uint4 q = reinterpret_cast<const uint4 *>(d + r * qb)[ch];
+            P[r * NC + j] = wi * arec_term(q, he, le, ho, lo, sx, X, to_f32(sd[r * ng + g]), to_f32(bd[r * ng + g]));
         }
     }
     __syncthreads();
-    for (int r = warp; r < nr; r += NW) {
+    for (int r = warp; r < nr; r += kDnThreads / 32) {
         float acc = 0.f;
         for (int q = lane; q < NC; q += 32)
             acc += P[r * NC + q];
-        acc = warp_sum(acc);
-        if (ready && lane == 0) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+        if (lane == 0) {
             A.y[h0 + r] = __float2bfloat16_rn(acc);
             if (A.y32)
                 A.y32[h0 + r] = acc;
@@ -1018,27 +939,35 @@ static int log2i(int v)
     return l;
 }
 
-// Gate/up units (8 row pairs) and 32-row chunks of a of one token.
-static int n_units(const Shape &s) { return s.Is / 8 + s.k * (s.I / 8); }
 static int n_chunks(const Shape &s) { return s.Is / 32 + s.k * (s.I / 32); }
+static int n_units(const Shape &s) { return s.Is / 8 + s.k * (s.I / 8); }
 
-// Dynamic shared memory of the experts kernel (the largest CTA share).
-static size_t experts_smem(const Shape &s, int n)
+// Dynamic shared memory of the down kernel (the largest CTA share).
+static size_t down_smem(const Shape &s, int n)
 {
     const size_t sb = s.qscale == MOE_F16 ? 2 : 4;
-    const size_t rowpair = (size_t)s.H + 4 * (size_t)(s.H / s.G) * sb; // gate and up code, scale and bias rows
-    const int units = (n_units(s) + n - 1) / n;
     const int nr = (s.H + n - 1) / n;
     size_t w = 0;
     for (int i = 0; i <= s.k; ++i) {
         const int inter = (i == s.k) ? s.Is : s.I;
         w += (size_t)nr * (inter / 2 + 2 * (inter / s.G) * sb);
     }
-    w = (w + 15) & ~(size_t)15;
-    return 8 * (size_t)units * rowpair + w + sizeof(float) * (size_t)nr * n_chunks(s);
+    w = (w + 127) & ~(size_t)127;
+    return w + (size_t)kArec * n_chunks(s) + sizeof(float) * (size_t)nr * n_chunks(s);
 }
 
-constexpr size_t kSmemLimit = 220 * 1024;
+// Dynamic shared memory of the gate/up kernel: the staged units of the
+// largest CTA share.
+static size_t gateup_smem(const Shape &s, int n)
+{
+    const size_t sb = s.qscale == MOE_F16 ? 2 : 4;
+    const size_t unitb = 8 * ((size_t)s.H + 4 * (size_t)(s.H / s.G) * sb);
+    return (size_t)((n_units(s) + n - 1) / n) * unitb;
+}
+
+// The gate/up and down kernels share an SM (with their static arrays, within
+// its 228 KB).
+constexpr size_t kSmemLimit = 196 * 1024;
 
 bool eligible(const Shape &s)
 {
@@ -1053,25 +982,15 @@ bool eligible(const Shape &s)
     const int sb = s.qscale == MOE_F16 ? 2 : 4;
     if (((s.H / s.G) * sb) % 16 || ((s.I / s.G) * sb) % 16 || ((s.Is / s.G) * sb) % 16)
         return false;
-    if (s.I % 32 || s.Is % 32 || s.G < 64) // one quantisation group per lane of a gate/up row
+    if (s.I % 32 || s.Is % 32 || s.G < 32)
         return false;
     const int n = sm_count();
-    const int units = (n_units(s) + n - 1) / n;
-    if (units > kMaxUnits || 8 * units > s.I || 8 * units > s.Is) // at most two segments per CTA
+    if ((n_units(s) + n - 1) / n > 5) // six copy lanes a unit, one warp
         return false;
-    if (2 * n_chunks(s) > kExThreads) // down: one thread per (chunk, half of the rows)
-        return false;
-    const int nr = (s.H + n - 1) / n;
-    if (nr > 2 * (kExThreads / 32)) // down: output rows per CTA
-        return false;
-    if (8 * units > kRowsPerWarp * (kExThreads / 32 - 1)) // gate/up row pairs per warp
-        return false;
-    if (12 + s.k + 1 > 32 || 6 * kMaxSeg * kParts > 12) // lanes of the copy warp
-        return false;
-    return experts_smem(s, n) <= kSmemLimit;
+    return gateup_smem(s, n) + down_smem(s, n) <= kSmemLimit;
 }
 
-// All three kernels run with the same (maximal) shared-memory carveout: an SM
+// All kernels run with the same (maximal) shared-memory carveout: an SM
 // whose L1/shared split would have to change between two of them must drain
 // first, which would serialise the PDL chain.
 template <typename F> static cudaError_t set_carveout(F *kern, bool *done)
@@ -1092,7 +1011,7 @@ size_t bufs_bytes(const Shape &s)
     const size_t lg = up256(sizeof(float) * (size_t)(s.E + 1));
     const size_t xr = up256((size_t)kRec * (s.H / 32));
     const size_t ar = up256((size_t)kArec * n_chunks(s));
-    return kRep * (lg + xr + ar) + 256;
+    return kRep * (lg + xr + ar);
 }
 
 Bufs bufs_carve(const Shape &s, char *base)
@@ -1107,13 +1026,11 @@ Bufs bufs_carve(const Shape &s, char *base)
     b.xrs = xr;
     b.arec = reinterpret_cast<unsigned char *>(base + kRep * (lg + xr));
     b.ars = ar;
-    b.bar = reinterpret_cast<unsigned int *>(base + kRep * (lg + xr + ar));
     return b;
 }
 
 cudaError_t launch_router(const Shape &s, const void *x, const void *w_router, const float *bias, const void *w_sg,
-                          float *lg, int lgs, int nrep, float *sg, unsigned char *xrec, size_t xrs, unsigned int *bar,
-                          cudaStream_t st)
+                          float *lg, int lgs, int nrep, float *sg, unsigned char *xrec, size_t xrs, cudaStream_t st)
 {
     const int rows = w_router ? s.E + (w_sg ? 1 : 0) : 0;
     const int row_ctas = (rows + 3) / 4;
@@ -1129,39 +1046,59 @@ cudaError_t launch_router(const Shape &s, const void *x, const void *w_router, c
         e = set_carveout(router_tok_kernel<4>, &cv4);
         return e != cudaSuccess ? e
                                 : launch_pdl(router_tok_kernel<4>, grid, 128, 0, st, xb, s.E, wr, bias, ws, lg, lgs,
-                                             nrep, sg, xrec, xrs, bar, row_ctas);
+                                             nrep, sg, xrec, xrs, row_ctas);
     }
     e = set_carveout(router_tok_kernel<8>, &cv8);
     return e != cudaSuccess ? e
                             : launch_pdl(router_tok_kernel<8>, grid, 128, 0, st, xb, s.E, wr, bias, ws, lg, lgs, nrep,
-                                         sg, xrec, xrs, bar, row_ctas);
+                                         sg, xrec, xrs, row_ctas);
 }
 
 template <int NXC, typename TS>
-static cudaError_t experts_go(const ExpertsArgs &A, int n, size_t smem, cudaStream_t st)
+static cudaError_t experts_go(const TokArgs &A, int n, size_t gsmem, size_t smem, int H, cudaStream_t st)
 {
-    static int cur = 0;
-    static bool cv = false;
-    cudaError_t e = set_carveout(experts_tok_kernel<NXC, TS>, &cv);
+    static int cur = 0, gcur = 0;
+    static bool cvg = false, cvd = false;
+    cudaError_t e = set_carveout(gateup_tok_kernel<NXC, TS>, &cvg);
     if (e == cudaSuccess)
-        e = ensure_smem(experts_tok_kernel<NXC, TS>, smem, &cur);
-    if (e != cudaSuccess)
-        return e;
-    return launch_pdl(experts_tok_kernel<NXC, TS>, n, kExThreads, smem, st, A);
+        e = set_carveout(down_tok_kernel<TS>, &cvd);
+    if (e == cudaSuccess)
+        e = ensure_smem(down_tok_kernel<TS>, smem, &cur);
+    if (e == cudaSuccess)
+        e = ensure_smem(gateup_tok_kernel<NXC, TS>, gsmem, &gcur);
+    if (e == cudaSuccess)
+        e = launch_pdl(gateup_tok_kernel<NXC, TS>, n, kGuThreads, gsmem, st, A);
+    if (e == cudaSuccess)
+        e = launch_pdl(down_tok_kernel<TS>, n, kDnThreads, smem, st, A, H);
+    return e;
 }
 
 cudaError_t launch_experts(const Shape &s, const Bufs &b, const ExpertSrc &src, const Routing &R, void *y,
                            float *y32, cudaStream_t st)
 {
     const int n = sm_count();
-    ExpertsArgs A{b.xrec, b.xrs, src, R, b.arec, b.ars, b.bar, static_cast<__nv_bfloat16 *>(y), y32,
-                  s.E, s.k, s.I, s.Is, log2i(s.G)};
-    const size_t smem = experts_smem(s, n);
+    TokArgs A{b.xrec, b.xrs, src, R, b.arec, b.ars, static_cast<__nv_bfloat16 *>(y), y32,
+              s.E, s.k, s.I, s.Is, log2i(s.G)};
+    const size_t smem = down_smem(s, n), gsmem = gateup_smem(s, n);
     const bool f16 = s.qscale == MOE_F16;
     if (s.H == 1024)
-        return f16 ? experts_go<1, __half>(A, n, smem, st) : experts_go<1, float>(A, n, smem, st);
-    return f16 ? experts_go<2, __half>(A, n, smem, st) : experts_go<2, float>(A, n, smem, st);
+        return f16 ? experts_go<1, __half>(A, n, gsmem, smem, s.H, st)
+                   : experts_go<1, float>(A, n, gsmem, smem, s.H, st);
+    return f16 ? experts_go<2, __half>(A, n, gsmem, smem, s.H, st) : experts_go<2, float>(A, n, gsmem, smem, s.H, st);
 }
 
 } // namespace tok
 } // namespace moe
+
+extern "C" moe_status moe_debug_set_waits(uint64_t wait_ns, int32_t extra_arrivals)
+{
+    using namespace moe;
+    if (wait_ns == 0 || extra_arrivals < 0 || extra_arrivals > 4)
+        return fail(MOE_ERR_INVALID_ARG, "moe_debug_set_waits: wait_ns > 0 and extra_arrivals in [0, 4]");
+    const unsigned long long w = wait_ns;
+    const int x = extra_arrivals;
+    cudaError_t e = cudaMemcpyToSymbol(tok::g_wait_ns, &w, sizeof(w));
+    if (e == cudaSuccess)
+        e = cudaMemcpyToSymbol(tok::g_extra_arrivals, &x, sizeof(x));
+    return cuda_check(e, "moe_debug_set_waits");
+}
