@@ -122,10 +122,9 @@ size_t moe_layer_workspace_bytes(const moe_config *cfg, int32_t T);
  *   in descending order; topk_w [T, k] fp32: exp(l_r - l_max) / sum over the
  *   k selected; shared_gate_logit [T] fp32 = w_shared_gate . x[t] (NULL iff no
  *   shared expert); logits_out [T, E] fp32 or NULL.  All device pointers.
- * For T >= 16 with bf16 x and router the logits are one cuBLAS bf16 GEMM
- * (fp32 accumulation).  The first such call on a device creates the
- * library's cuBLAS handle, which allocates device memory: make it outside
- * stream capture.  moe_layer_forward_noalloc never takes this route. */
+ * For T >= 16 with bf16 x and router the logits and the shared-gate logit
+ * are one bf16 tensor-core GEMM of the library's own (fp32 accumulation);
+ * the library calls no BLAS. */
 moe_status moe_route(const moe_config *cfg, const void *x, int32_t T, const void *w_router,
                      const float *router_bias, const void *w_shared_gate, int32_t *topk_idx,
                      float *topk_w, float *shared_gate_logit, float *logits_out,
@@ -193,15 +192,18 @@ moe_status moe_layer_forward(const moe_config *cfg, const moe_layer *layer, cons
  * cudaMalloc's implicit synchronisation).  The Swiftlet pages have no
  * counterpart; this is an interface convenience.
  * Scratch is a 4 MiB array built into the library's device image, held by
- * every GPU that loads the library until the process exits; T is limited to
- * what fits (moe_layer_workspace_bytes(cfg, T) <= 4 MiB, about T <= 160 for
- * the 80B shape), larger T returns MOE_ERR_OOM.  Nothing is allocated: no
- * cudaMalloc, cudaFree or allocating library call.  The first call on each
- * device looks up the array's device address (cudaGetSymbolAddress) with
- * that device current; make that first call before any stream capture.  All
- * calls on a device share the one array and it keeps the last call's
- * contents; calls whose GPU work overlaps race on it, so order them (one
- * stream, or events).  Other arguments and behaviour as moe_layer_forward. */
+ * every GPU that loads the library until the process exits.  T is limited to
+ * what fits: moe_layer_workspace_bytes(cfg, T) <= 4 MiB, which for the 35B-
+ * and 80B-shaped layers means T <= 63 (from T = 64 on the grouped-GEMM
+ * buffers alone exceed it); larger T returns MOE_ERR_OOM.  Nothing is
+ * allocated: no cudaMalloc, cudaFree or allocating library call.  The first
+ * call on a device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current; make that first call before any stream capture.
+ * The library as a whole serves one GPU per process (its kernels' attributes
+ * are set once per process), so call it from one device only.
+ * All calls share the one array and it keeps the last call's contents; calls
+ * whose GPU work overlaps race on it, so order them (one stream, or events).
+ * Other arguments and behaviour as moe_layer_forward. */
 moe_status moe_layer_forward_noalloc(const moe_config *cfg, const moe_layer *layer, const void *x,
                                      int32_t T, void *y, float *y_f32, int32_t *topk_idx_out,
                                      float *topk_w_out, cudaStream_t stream);
@@ -259,7 +261,13 @@ moe_status slot_pool_lookup(slot_pool *p, int32_t layer, const int32_t *expert_i
 /* Enqueue on the side stream one host->device copy per missed expert into
  * its slot and the matching device-table update, then record `done` (may be
  * NULL).  Work on another stream that reads the layer's slots must wait on
- * `done`.  The miss list is the one the last lookup of this layer returned. */
+ * `done`.  The copies overwrite the evicted experts' slots: every earlier
+ * reader of those slots (kernels on any stream that used the layer's table
+ * before this lookup) must have completed before slot_pool_fill is called,
+ * or the side stream must be made to wait for them (an event recorded after
+ * the last reader, cudaStreamWaitEvent on side_stream).
+ * moe_pooled_layer_forward orders this itself.  The miss list is the one the
+ * last lookup of this layer returned. */
 moe_status slot_pool_fill(slot_pool *p, int32_t layer, const int32_t *miss_ids, int32_t n_miss,
                           cudaEvent_t done);
 

@@ -38,7 +38,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     tmp = LIB + f".{os.getpid()}.tmp"
     cmd = [NVCC, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
            "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC,
-           os.path.join(CSRC, "lib.cu"), "-o", tmp, "-lcudart", "-lcublas"]
+           os.path.join(CSRC, "lib.cu"), "-o", tmp, "-lcudart"]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     subprocess.check_call(cmd)

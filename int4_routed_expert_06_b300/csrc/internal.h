@@ -25,19 +25,12 @@ moe_status check_config(const moe_config *c, Shape *s);
 cudaError_t launch_router(const Shape &s, const void *x, int T, const void *w_router,
                           const float *bias, const void *w_sg, float *logits, float *sg_logit,
                           cudaStream_t st);
-// Calls with at least this many tokens compute the router logits as one
-// cuBLAS bf16 GEMM (fp32 accumulation) plus a bias / shared-gate kernel.
+// Calls with at least this many tokens compute the router logits (and the
+// shared-gate logit) as one bf16 tensor-core GEMM with fp32 accumulation.
 constexpr int kRouterGemmMinTokens = 16;
 bool router_gemm_eligible(const Shape &s, int T);
 cudaError_t launch_router_gemm(const Shape &s, const void *x, int T, const void *w_router, const float *bias,
                                const void *w_sg, float *logits, float *sg_logit, cudaStream_t st);
-// While one of these lives on a thread, the library makes no call that may
-// allocate device memory (moe_layer_forward_noalloc).
-struct NoAllocScope {
-    NoAllocScope();
-    ~NoAllocScope();
-};
-bool in_no_alloc_scope();
 // Top-k + renormalised softmax from logits [T, E].
 cudaError_t launch_topk(const Shape &s, const float *logits, int T, int32_t *idx, float *w,
                         cudaStream_t st);

@@ -57,7 +57,8 @@ constexpr int kRec = 80;       // bytes per fixed-point chunk record
 constexpr int kGuWarps = 16;
 constexpr int kGuThreads = 32 * kGuWarps;
 constexpr int kMaxUnits = 5;   // gate/up units (8 row pairs) a CTA stages: 6 copy lanes each
-constexpr int kDnThreads = 256;
+constexpr int kDnThreads = 384;
+constexpr int kMaxRH = 8;      // output rows a down thread computes (half of a CTA's rows)
 
 // Bound on every device wait (ns) and extra arrivals the down kernel's copy
 // barrier expects.  Both are test hooks (moe_debug_set_waits): the defaults
@@ -296,7 +297,8 @@ struct TopkBlk {
 
 // Top k of the E <= EPT NT logits at lg (global memory, written by an earlier
 // kernel) by all threads of the CTA; thread t < NT holds experts t + NT j
-// (NT a power of two, at least 32; threads past NT hold none).
+// (NT a power of two, at least 32; threads past NT hold none).  At most 32
+// warps.
 //
 // The keys are cut into 32 groups of NT / 32 consecutive threads.  T = the
 // group maximum of the largest rank <= k - 1 is at most the k-th largest key
@@ -562,12 +564,12 @@ __device__ __forceinline__ void named_sync(int id, int nthreads)
 // lanes 0..7 of the group's first warp write the unit's quarter of its
 // chunk's activation record, one copy each.
 //
-// 80 registers a thread: with the down kernel (256 x 64) and the router (128
+// 72 registers a thread: with the down kernel (384 x 56) and the router (128
 // x 56) beside it, each of the SM's four register banks holds its share of
 // all three kernels, so each kernel's CTAs are resident before its
 // predecessor ends.
 template <int NXC, typename TS>
-__global__ void __maxnreg__(80) gateup_tok_kernel(TokArgs A)
+__global__ void __maxnreg__(72) gateup_tok_kernel(TokArgs A)
 {
     constexpr int H = 1024 * NXC;
     constexpr int NG = kGuWarps / 4; // warp groups
@@ -638,12 +640,15 @@ __global__ void __maxnreg__(80) gateup_tok_kernel(TokArgs A)
         bulk_g2s(xs, A.xrec + (size_t)rep * A.xrs, xb, &xbar);
     }
     load_routing<kGuThreads>(A.R, rep, A.E, k, tks, s_idx, nullptr, false);
-    if ((int)threadIdx.x < k)
-        s_base[threadIdx.x] = routed_base(A.src, tab, s_idx[threadIdx.x]);
-    __syncthreads();
-    if (warp == kGuWarps - 1)
+    // the staging warp resolves the slots; compute warps read s_base only
+    // after a unit barrier it armed (its arrival releases these writes)
+    if (warp == kGuWarps - 1) {
+        if (lane < k)
+            s_base[lane] = routed_base(A.src, tab, s_idx[lane]);
+        __syncwarp();
         for (int j = js; j < min(nu, js + kDepth); ++j)
             stage(j);
+    }
 
     // ---- gate/up: this lane's chunks of x, then the group's units
     const bool xok = __all_sync(0xFFFFFFFFu, mbar_wait0(&xbar));
@@ -655,7 +660,8 @@ __global__ void __maxnreg__(80) gateup_tok_kernel(TokArgs A)
     for (int j = grp; j < nu; j += NG) {
         int i, o0;
         unit_of(u0 + j, k, A.I, A.Is, &i, &o0);
-        const bool have = xok && s_base[i] != nullptr && __all_sync(0xFFFFFFFFu, mbar_wait0(&ubar[j]));
+        const bool landed = __all_sync(0xFFFFFFFFu, mbar_wait0(&ubar[j]));
+        const bool have = xok && landed && s_base[i] != nullptr;
         if (wq == 0 && j >= js && j + kDepth < nu)
             stage(j + kDepth);
         const unsigned char *d = units + (size_t)j * unitb;
@@ -754,15 +760,18 @@ __device__ __forceinline__ float arec_term(uint4 q, uint4 he, uint4 le, uint4 ho
 
 // Down projection and combine.  CTA c computes output rows [h0, h1) =
 // [c H / n, (c + 1) H / n).  Its W_d rows of every active expert (codes
-// [nr][I_i/2], then scales and biases [nr][I_i/G] each, per expert; L2-warm
-// from the gate/up kernel's prefetch) and the activation records are bulk-
-// copied into shared memory; thread t owns chunks t, t + kDnThreads, ... of
-// the chunk list [shared | rank 0 | rank 1 | ...]: it writes w_i times its
-// chunk's term of each output row to P[row][chunk].  Warps then sum each row
-// over the chunks in a fixed order, so the result does not depend on where
-// the experts live.  The routing (with weights) is computed before the wait.
+// [nr][I_i/2], then scales and biases [nr][I_i/G] each, per expert) are bulk-
+// copied into shared memory before the wait (weights: not written by the
+// kernels this one waits for), the activation records after it.  Thread t
+// takes chunk t % NCp of the chunk list [shared | rank 0 | rank 1 | ...]
+// (NCp = the chunk count rounded up to 32) for half t / NCp of the output
+// rows, and forms w_i times its chunk's term of each of those rows.  Each
+// warp sums every row over its 32 chunks by butterfly, then one thread a row
+// adds its half's warps in order: a fixed summation order, so the result does
+// not depend on where the experts live.  The routing (with weights) is
+// computed before the wait.
 template <typename TS>
-__global__ void __maxnreg__(64) down_tok_kernel(TokArgs A, int H)
+__global__ void __maxnreg__(56) down_tok_kernel(TokArgs A, int H)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint64_t dbar, rbar;
@@ -772,6 +781,7 @@ __global__ void __maxnreg__(64) down_tok_kernel(TokArgs A, int H)
     __shared__ float s_w[kMaxAct + 1];
     __shared__ const char *s_base[kMaxAct];
     __shared__ uint32_t s_eoff[kMaxAct + 1]; // offset of expert i's rows in the down region
+    __shared__ float Pw[2 * kMaxRH][kDnThreads / 32]; // [row][warp] partial sums
 
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int n = gridDim.x, c = blockIdx.x, rep = c % kRep;
@@ -796,7 +806,7 @@ __global__ void __maxnreg__(64) down_tok_kernel(TokArgs A, int H)
     }
     for (int e = t; e < A.E; e += kDnThreads)
         tab[e] = __ldg(A.src.table + e);
-    load_routing<kDnThreads>(A.R, rep, A.E, k, tks, s_idx, s_w, false);
+    load_routing<256>(A.R, rep, A.E, k, tks, s_idx, s_w, false); // keys on the first 256 threads
     if (t < k)
         s_base[t] = routed_base(A.src, tab, s_idx[t]);
     if (t == 32)
@@ -807,7 +817,6 @@ __global__ void __maxnreg__(64) down_tok_kernel(TokArgs A, int H)
     // by the kernels this one waits for, so copied before the wait)
     unsigned char *down = smem;
     unsigned char *rec = smem + ((s_eoff[n_act] + 127) & ~127u); // [NC][kArec]
-    float *P = reinterpret_cast<float *>(rec + (size_t)NC * kArec); // [nr][NC]
     if (warp == 0) {
         const char *b = lane < n_act ? s_base[lane] : nullptr;
         const int inter = lane == k ? A.Is : A.I;
@@ -848,8 +857,16 @@ __global__ void __maxnreg__(64) down_tok_kernel(TokArgs A, int H)
         mbar_wait0(&dbar);
     ready = __syncthreads_and(ready && rec_ok);
 
-    // ---- per-chunk terms of every output row
-    for (int j = t; j < NC; j += kDnThreads) {
+    // ---- the terms: thread t, chunk j = t % NCp, rows [r0, r0 + nrr) of half hf
+    const int NCp = (NC + 31) & ~31;
+    const int RH = (nr + 1) >> 1;
+    const int hf = t / NCp, j = t - hf * NCp;
+    const int r0 = hf * RH, nrr = hf < 2 ? max(0, min(nr, r0 + RH) - r0) : 0; // uniform across a warp
+    float v[kMaxRH];
+#pragma unroll
+    for (int rr = 0; rr < kMaxRH; ++rr)
+        v[rr] = 0.f;
+    if (ready && hf < 2 && j < NC && nrr > 0) {
         int i, ch;
         if (j < (A.Is >> 5)) {
             i = k;
@@ -858,43 +875,54 @@ __global__ void __maxnreg__(64) down_tok_kernel(TokArgs A, int H)
             i = (j - (A.Is >> 5)) / (A.I >> 5);
             ch = (j - (A.Is >> 5)) - i * (A.I >> 5);
         }
-        if (!ready || !s_base[i]) {
-            for (int r = 0; r < nr; ++r)
-                P[r * NC + j] = 0.f;
-            continue;
+        if (s_base[i]) {
+            const uint4 *rv = reinterpret_cast<const uint4 *>(rec + (size_t)j * kArec);
+            const uint4 he = rv[0], le = rv[1], ho = rv[2], lo = rv[3], sxu = rv[4], Xu = rv[5];
+            const float4 sx = make_float4(__uint_as_float(sxu.x), __uint_as_float(sxu.y), __uint_as_float(sxu.z),
+                                          __uint_as_float(sxu.w));
+            const float4 X = make_float4(__uint_as_float(Xu.x), __uint_as_float(Xu.y), __uint_as_float(Xu.z),
+                                         __uint_as_float(Xu.w));
+            const int inter = i == k ? A.Is : A.I;
+            const int qb = inter / 2, ng = inter >> A.log2G;
+            const unsigned char *d = down + s_eoff[i];
+            const TS *sd = reinterpret_cast<const TS *>(d + nr * qb);
+            const TS *bd = sd + nr * ng;
+            const int g = (ch * 32) >> A.log2G;
+            const float wi = i < k ? s_w[i] : s_w[kMaxAct];
+            // straight-line over kMaxRH rows (rows past this half repeat its
+            // last row and are dropped), so the rows' chains interleave
+#pragma unroll
+            for (int rr = 0; rr < kMaxRH; ++rr) {
+                const int r = r0 + min(rr, nrr - 1);
+                const uint4 q = reinterpret_cast<const uint4 *>(d + r * qb)[ch];
+                const float term =
+                    wi * arec_term(q, he, le, ho, lo, sx, X, to_f32(sd[r * ng + g]), to_f32(bd[r * ng + g]));
+                v[rr] = rr < nrr ? term : 0.f;
+            }
         }
-        const uint4 *rv = reinterpret_cast<const uint4 *>(rec + (size_t)j * kArec);
-        const uint4 he = rv[0], le = rv[1], ho = rv[2], lo = rv[3], sxu = rv[4], Xu = rv[5];
-        const float4 sx = make_float4(__uint_as_float(sxu.x), __uint_as_float(sxu.y), __uint_as_float(sxu.z),
-                                      __uint_as_float(sxu.w));
-        const float4 X = make_float4(__uint_as_float(Xu.x), __uint_as_float(Xu.y), __uint_as_float(Xu.z),
-                                     __uint_as_float(Xu.w));
-        const int inter = i == k ? A.Is : A.I;
-        const int qb = inter / 2, ng = inter >> A.log2G;
-        const unsigned char *d = down + s_eoff[i];
-        const TS *sd = reinterpret_cast<const TS *>(d + nr * qb);
-        const TS *bd = sd + nr * ng;
-        const int g = (ch * 32) >> A.log2G;
-        const float wi = i < k ? s_w[i] : s_w[kMaxAct];
-#pragma unroll 4
-        for (int r = 0; r < nr; ++r) {
-            const uint4 q = reinterpret_cast<const uint4 *>(d + r * qb)[ch];
-            P[r * NC + j] = wi * arec_term(q, he, le, ho, lo, sx, X, to_f32(sd[r * ng + g]), to_f32(bd[r * ng + g]));
+    }
+    // ---- per warp, each row's sum over the warp's chunks; then per row, its
+    // half's warps in order
+#pragma unroll
+    for (int rr = 0; rr < kMaxRH; ++rr) {
+        if (rr < nrr) {
+            float x = v[rr];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+            if (lane == 0)
+                Pw[r0 + rr][warp] = x;
         }
     }
     __syncthreads();
-    for (int r = warp; r < nr; r += kDnThreads / 32) {
+    if (t < nr) {
+        const int wpr = NCp / 32, w0 = (t >= RH ? 1 : 0) * wpr; // warps of each half
         float acc = 0.f;
-        for (int q = lane; q < NC; q += 32)
-            acc += P[r * NC + q];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-        if (lane == 0) {
-            A.y[h0 + r] = __float2bfloat16_rn(acc);
-            if (A.y32)
-                A.y32[h0 + r] = acc;
-        }
+        for (int w = w0; w < w0 + wpr; ++w)
+            acc += Pw[t][w];
+        A.y[h0 + t] = __float2bfloat16_rn(acc);
+        if (A.y32)
+            A.y32[h0 + t] = acc;
     }
 }
 
@@ -953,7 +981,7 @@ static size_t down_smem(const Shape &s, int n)
         w += (size_t)nr * (inter / 2 + 2 * (inter / s.G) * sb);
     }
     w = (w + 127) & ~(size_t)127;
-    return w + (size_t)kArec * n_chunks(s) + sizeof(float) * (size_t)nr * n_chunks(s);
+    return w + (size_t)kArec * n_chunks(s);
 }
 
 // Dynamic shared memory of the gate/up kernel: the staged units of the
@@ -986,6 +1014,9 @@ bool eligible(const Shape &s)
         return false;
     const int n = sm_count();
     if ((n_units(s) + n - 1) / n > 5) // six copy lanes a unit, one warp
+        return false;
+    // down: two threads (row halves) to each chunk, rounded up to whole warps
+    if (2 * ((n_chunks(s) + 31) & ~31) > kDnThreads || (s.H + n - 1) / n > 2 * kMaxRH)
         return false;
     return gateup_smem(s, n) + down_smem(s, n) <= kSmemLimit;
 }

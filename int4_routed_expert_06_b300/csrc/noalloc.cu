@@ -67,7 +67,6 @@ extern "C" moe_status moe_layer_forward_noalloc(const moe_config *cfg, const moe
         }
         scratch = g_noalloc_ptr[dev];
     }
-    NoAllocScope no_alloc; // no cuBLAS handle (it allocates) on this path
     return moe_layer_forward(cfg, layer, x, T, y, y_f32, topk_idx_out, topk_w_out, scratch, kNoAllocScratchBytes,
                              stream);
 }

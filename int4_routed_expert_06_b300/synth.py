@@ -55,10 +55,11 @@ class MoEShape:
     layers: int = 1
     pool_slots: int = 0   # slots per layer in a bounded pool (0 = all resident)
     weight_seed: int = 0
+    router_on_grid: bool = False  # router and shared gate drawn, then put on the affine 4-bit grid
 
 
 TINY = MoEShape("tiny", 64, 8, 2, 32, 32, 32, "f32", "f32", "f32", 0.05, 0.05,
-                tokens=4, weight_seed=0)
+                tokens=4, weight_seed=0, router_on_grid=True)
 DEC_35B = MoEShape("35b-dec", 2048, 256, 8, 512, 512, 64, "bf16", "bf16", "f16",
                    0.02, 0.02, weight_seed=1)
 DEC_80B = MoEShape("80b-dec", 2048, 512, 10, 512, 512, 64, "bf16", "bf16", "f16",
@@ -167,15 +168,37 @@ def zipf_router_bias(shape: MoEShape, seed: int, device="cpu") -> Optional[torch
     return bias.to(torch.float32).to(device)
 
 
+def on_affine4_grid(w: torch.Tensor, group: int) -> torch.Tensor:
+    """The dense fp32 values a checkpoint holds for w after min-max affine 4-bit
+    quantisation with groups of `group` along the last dim (s * q + b for
+    each weight).  A checkpoint-preparation step for weights the layer then
+    reads as dense fp32 (the router and shared gate of the workload whose
+    weights are all quantised); the layer's own int4 path never calls it."""
+    *lead, n = w.shape
+    g = w.reshape(*lead, n // group, group)
+    lo = g.amin(dim=-1, keepdim=True)
+    scale = (g.amax(dim=-1, keepdim=True) - lo) / 15.0
+    safe = torch.where(scale > 0, scale, torch.ones_like(scale))
+    code = torch.where(scale > 0, torch.round((g - lo) / safe), torch.zeros_like(g)).clamp_(0, 15)
+    return (code * scale + lo).reshape(w.shape)
+
+
 def make_router(shape: MoEShape, seed: Optional[int] = None, device="cpu") -> Dict[str, torch.Tensor]:
     """The resident routing weights of a layer, exactly as make_layer draws
-    them: w_router [E,H], w_shared_gate [H], router_bias [E] fp32 or None."""
+    them: w_router [E,H], w_shared_gate [H], router_bias [E] fp32 or None.
+    With shape.router_on_grid the draws are first put on the affine 4-bit
+    grid (group shape.group) and kept as dense values."""
     seed = shape.weight_seed if seed is None else seed
     gen = _gen(seed, device)
     rd = torch_dtype(shape.router)
+    wr = _randn((shape.n_experts, shape.hidden), shape.router_std, gen, device)
+    wsg = _randn((shape.hidden,), shape.router_std, gen, device)
+    if shape.router_on_grid:
+        wr = on_affine4_grid(wr, shape.group)
+        wsg = on_affine4_grid(wsg, shape.group)
     return {
-        "w_router": _randn((shape.n_experts, shape.hidden), shape.router_std, gen, device).to(rd),
-        "w_shared_gate": _randn((shape.hidden,), shape.router_std, gen, device).to(rd),
+        "w_router": wr.to(rd),
+        "w_shared_gate": wsg.to(rd),
         "router_bias": zipf_router_bias(shape, seed, device),
     }
 

@@ -146,3 +146,21 @@ def test_strided_tensors_are_refused_before_any_call():
     x = torch.zeros((4, 2 * synth.DEC_80B.hidden), dtype=torch.bfloat16)[:, ::2]
     with pytest.raises(ValueError):
         B.moe_layer_forward(cfg, B.moe_layer(), x, 4, None, stream=0)
+
+
+def test_debug_wait_hook_validates_before_touching_a_device():
+    with pytest.raises(B.MoEError) as ei:
+        B.moe_debug_set_waits(0, 0)
+    assert ei.value.status == B.MOE_ERR_INVALID_ARG
+    with pytest.raises(B.MoEError) as ei:
+        B.moe_debug_set_waits(1_000_000, 5)
+    assert ei.value.status == B.MOE_ERR_INVALID_ARG
+
+
+def test_noalloc_scratch_bound_stated_in_the_header():
+    """The header states T <= 63 for the 35B- and 80B-shaped layers: the
+    built-in 4 MiB scratch holds the single-token and generic paths' buffers,
+    and from T = 64 on the grouped-GEMM buffers alone exceed it."""
+    for shape in (synth.DEC_35B, synth.DEC_80B):
+        cfg = B.config_for(shape)
+        assert B.moe_layer_workspace_bytes(cfg, 63) <= 4 << 20 < B.moe_layer_workspace_bytes(cfg, 64)

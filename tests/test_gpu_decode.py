@@ -93,26 +93,45 @@ def kernel_path():
     B.moe_set_kernel_path(0)
 
 
+def _decode_sample(n_first=50, n_random=50, steps=1000, seed=77):
+    """Decode steps checked: the first n_first of the seeded sequence and
+    n_random more drawn (seeded) from the rest."""
+    rng = np.random.default_rng(seed)
+    rest = rng.choice(np.arange(n_first, steps), size=n_random, replace=False)
+    return list(range(n_first)) + sorted(int(s) for s in rest)
+
+
 @pytest.mark.parametrize("path", [0, 1])
 @pytest.mark.parametrize("name", NAMES)
 def test_layer_decode_parity(name, path, kernel_path):
     """T = 1 decode steps, each its own call (the bench's configuration), on
-    the fast single-token kernels and on the generic ones."""
+    the fast single-token kernels and on the generic ones: the tiny layer's
+    tokens, and for the 35B- and 80B-shaped layers the first 50 steps of the
+    seeded decode sequence plus 50 seeded random ones from the rest of its
+    1000.  Routing must match the oracle exactly except on near-tie steps
+    (gap between the k-th and (k+1)-th oracle logit within 1e-4 max(1, |l_k|)),
+    which are counted: at most 2 of 100."""
     kernel_path(path)
     shape, w, L = layer_of(name)
     dl = device_layer(name)
-    xs = _xs(name, 6)
-    steps = range(len(xs)) if name == "tiny" else range(6)
+    if name == "tiny":
+        xs = _xs(name, 4)
+        steps = list(range(len(xs)))
+    else:
+        xs = synth.decode_xs(shape, 1000, device="cuda")
+        steps = _decode_sample()
+    ties = 0
     for s in steps:
         x = xs[s:s + 1]
         y, y32, idx, tw = layer_forward(dl, x)
         ref = L.forward(x)
-        tie = near_tie_tokens(ref["logits"], shape.top_k)
-        if tie[0]:
+        if near_tie_tokens(ref["logits"], shape.top_k)[0]:
+            ties += 1
             continue
-        np.testing.assert_array_equal(idx.cpu().numpy(), ref["idx"])
+        np.testing.assert_array_equal(idx.cpu().numpy(), ref["idx"], err_msg=f"{name} step {s}")
         assert_close(y32.cpu().numpy(), ref["y"], shape.act, f"{name} step {s} y_f32")
         assert_close(y.float().cpu().numpy(), ref["y"], shape.act, f"{name} step {s} y")
+    assert ties <= 2, f"{ties} near-tie steps of {len(steps)}"
 
 
 @pytest.mark.parametrize("name,T", [("tiny", 4), ("35b-dec", 5), ("80b-dec", 3)])

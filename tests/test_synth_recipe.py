@@ -45,3 +45,18 @@ def test_quantiser_codes_in_range_and_deterministic():
     assert q.dtype == torch.int32 and q.shape == (8, 32, 8)
     t = synth.shuffled_slots(512, 2)
     assert sorted(t.tolist()) == list(range(512))
+
+
+def test_tiny_router_and_shared_gate_lie_on_the_affine4_grid():
+    """The tiny workload quantises all its weights: its router and shared-gate
+    rows, kept dense, hold at most 16 equally spaced values per group of 32
+    (s * q + b with q in 0..15)."""
+    shp = synth.TINY
+    r = synth.make_router(shp)
+    for wmat in (r["w_router"], r["w_shared_gate"][None]):
+        g = wmat.double().reshape(-1, shp.group)
+        lo = g.min(dim=1, keepdim=True).values
+        step = (g.max(dim=1, keepdim=True).values - lo) / 15.0
+        q = (g - lo) / step
+        assert torch.allclose(q, q.round(), atol=1e-4)
+        assert int(q.round().max()) <= 15 and int(q.round().min()) >= 0
