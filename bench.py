@@ -23,6 +23,9 @@ at batch 1); no collective touches the data path.
 
 `--impl reference` times the CPU oracle instead (rank 0 only).
 
+`--workload 35b-dec`, `80b-dec-int8` and `35b-dec-int8` time the same decode
+loop on the 35B-shaped layer and on both layers with affine int8 codes.
+
 Two more workloads print their own line (not the default):
 
 - `--workload 80b-prefill`: one step = one 4096-token layer call (Zipf-skewed
@@ -65,7 +68,8 @@ def metric_of(shape) -> str:
                 f"top-{shape.top_k} int4, Zipf-skewed routing)")
     if shape.name == "80b-stack":
         return "80B-stack decode tokens/s through a bounded HBM expert pool (25% of experts per layer)"
-    return f"routed-MoE layer tokens/s (decode, {shape.n_experts}e top-{shape.top_k} int4); HBM GB/s vs peak"
+    return (f"routed-MoE layer tokens/s (decode, {shape.n_experts}e top-{shape.top_k} int{shape.bits}); "
+            "HBM GB/s vs peak")
 
 
 assert metric_of(synth.DEC_80B) == METRIC
@@ -95,8 +99,8 @@ def recorded_traffic(workload: str):
         with open(rec) as f:
             for line in f:
                 parts = line.split()
-                if len(parts) == 5 and not line.startswith("#") and parts[0] == workload:
-                    return int(parts[4]) if parts[1] == digest else None
+                if len(parts) >= 5 and not line.startswith("#") and parts[0] == workload:
+                    return int(parts[-1]) if parts[1] == digest else None
     except OSError:
         return None
     return None
@@ -111,7 +115,7 @@ def workload_desc(shape) -> str:
     else:
         mode = "batch-1 decode"
     return (f"{shape.name}: routed MoE layer H={shape.hidden} E={shape.n_experts} top-{shape.top_k} "
-            f"I={shape.inter} shared I={shape.shared_inter} sigmoid-gated, int4 affine g{shape.group} "
+            f"I={shape.inter} shared I={shape.shared_inter} sigmoid-gated, int{shape.bits} affine g{shape.group} "
             f"{shape.qscale} scale/bias, {shape.act} x/y, {mode}")
 
 
@@ -189,17 +193,44 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- CPU oracle
 
-def oracle_tokens_per_s(layer_w, shape, xs, budget_s: float, max_tokens: int):
-    """Time the CPU oracle on the first tokens of the seeded decode sequence."""
+def host_cores() -> int:
+    """Cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def oracle_tokens_per_s(layer_w, shape, xs, budget_s: float, max_tokens: int, threads: int = 1):
+    """Time the CPU oracle on the first tokens of xs (one token a call), its
+    loops over output rows on `threads` threads."""
     from oracle import oracle as O
-    L = O.Layer(layer_w, shape.group, shape.top_k)
-    L.forward(xs[:1])  # compile / load outside the clock
-    n, t0 = 0, time.perf_counter()
-    while n < max_tokens and (time.perf_counter() - t0) < budget_s:
-        L.forward(xs[n:n + 1])
-        n += 1
-    dt = time.perf_counter() - t0
+    O.set_threads(threads)
+    try:
+        L = O.Layer(layer_w, shape.group, shape.top_k)
+        L.forward(xs[:1])  # compile / load outside the clock
+        n, t0 = 0, time.perf_counter()
+        while n < max_tokens and (time.perf_counter() - t0) < budget_s:
+            L.forward(xs[n:n + 1])
+            n += 1
+        dt = time.perf_counter() - t0
+    finally:
+        O.set_threads(1)
     return n / dt, n, dt
+
+
+def cpu_baseline_of(layer_w, shape, xs, budget_s: float, max_tokens: int, what: str, per_token_factor: float = 1.0):
+    """The oracle on all available host cores (OpenMP over output rows) and on
+    one core, each on a bounded sample of xs; tokens/s divided by
+    per_token_factor (the layers a token passes through)."""
+    cores = host_cores()
+    v, n, dt = oracle_tokens_per_s(layer_w, shape, xs, budget_s / 2, max_tokens, threads=cores)
+    v1, n1, dt1 = oracle_tokens_per_s(layer_w, shape, xs, budget_s / 2, max_tokens, threads=1)
+    return {"value": v / per_token_factor, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{what}: {n} tokens in {dt:.1f} s on {cores} cores (plain C, fp64, OpenMP over output "
+                      f"rows)",
+            "single_thread": {"value": v1 / per_token_factor, "cores": 1,
+                              "sample": f"{n1} tokens in {dt1:.1f} s on one core"}}
 
 
 def run_reference(args, shape, rank):
@@ -213,6 +244,8 @@ def run_reference(args, shape, rank):
     else:
         xs = synth.decode_xs(shape, n, device=dev)
     from oracle import oracle as O
+    cores = host_cores()
+    O.set_threads(cores)
     L = O.Layer(w, shape.group, shape.top_k)
     for j in range(args.warmup):
         L.forward(xs[j:j + 1])
@@ -220,6 +253,7 @@ def run_reference(args, shape, rank):
     for j in range(args.steps):
         L.forward(xs[args.warmup + j:args.warmup + j + 1])
     dt = time.perf_counter() - t0
+    O.set_threads(1)
     # a stack token is one pass through every layer: the oracle's per-layer
     # rate divided by the layer count (layer 0's weights stand for all)
     v = args.steps / dt / max(shape.layers, 1)
@@ -229,8 +263,10 @@ def run_reference(args, shape, rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": workload_desc(shape), "tokens_per_step": 1,
                                         "l2": "n/a (host)"},
-        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{args.steps} seeded decode tokens (x seeds {synth.DECODE_X_SEED0 + args.warmup}+)"},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} seeded tokens, one a call, OpenMP over output rows on {cores} "
+                                   f"cores" + (" (layer 0's weights stand for each of the stack's layers)"
+                                               if shape.layers > 1 else "")},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
@@ -301,6 +337,11 @@ def run_prefill(args, shape):
         e1.record(stream)
     torch.cuda.synchronize()
     e2e = n_e2e * T / (e0.elapsed_time(e1) * 1e-3)
+    cpu = None
+    if not args.no_cpu_baseline:  # per token, on a bounded sample of the batch (the layer is per-token)
+        cpu = cpu_baseline_of(w, shape, x, args.cpu_seconds, 200,
+                              f"first tokens of the {T}-token batch, one a call; tokens/s of the batch "
+                              "extrapolated per token")
     print(json.dumps({
         "metric": metric_of(shape),
         "value": T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
@@ -318,6 +359,7 @@ def run_prefill(args, shape):
                      "frac": tf / pk[0], "traffic": None, "algorithmic_flops_per_launch": flops},
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": xh.numel() * 2,
                 "d2h_bytes_per_step": yh.numel() * 2},
+        "cpu_baseline": cpu,
         "clocks": clk.summary(),
     }), flush=True)
 
@@ -334,6 +376,17 @@ def peak_bf16():
 
 
 # ---------------------------------------------------------------- stack
+
+def layer_input(x: torch.Tensor, eps: float = 1e-6) -> torch.Tensor:
+    """The input of the next MoE layer in the stack workload: the residual
+    stream x [T, H] scaled to unit RMS per token (fp32 arithmetic, result in
+    x's dtype).  Workload chaining, not layer arithmetic: without a norm
+    between layers the SwiGLU experts, whose output grows with the square of
+    their input, drive a residual chain of random layers to overflow within a
+    few dozen layers."""
+    xf = x.float()
+    return (xf * torch.rsqrt(xf.pow(2).mean(dim=-1, keepdim=True) + eps)).to(x.dtype)
+
 
 def host_bytes_available() -> int:
     avail = 0
@@ -359,7 +412,7 @@ def host_bytes_available() -> int:
 def run_stack(args, shape):
     from int4_routed_expert_06_b300 import binding as B
     from int4_routed_expert_06_b300 import build as _build
-    from int4_routed_expert_06_b300.stack import PooledStack, layer_input
+    from int4_routed_expert_06_b300.stack import PooledStack
     _build.build()
     torch.cuda.set_device(0)
     E, k = shape.n_experts, shape.top_k
@@ -369,10 +422,13 @@ def run_stack(args, shape):
     if fit < L:
         L = max(1, fit)
     resident = []
+    first = {}
 
     def weights(l):
         w = synth.make_layer(shape, seed=shape.weight_seed + l, device="cuda")
         resident.append(B.DeviceLayer(shape, w, torch.arange(E, dtype=torch.int32)))
+        if l == 0:
+            first["w"] = w
         return w
 
     t_build = time.perf_counter()
@@ -440,6 +496,12 @@ def run_stack(args, shape):
     torch.cuda.synchronize()
     h2d_gbs = 64 * blob / (c0.elapsed_time(c1) * 1e-3) / 1e9
     K = args.steps
+    cpu = None
+    if not args.no_cpu_baseline:  # layer 0's oracle per layer-token, over the stack's layers
+        xin = torch.cat([layer_input(x0[j:j + 1]) for j in range(min(n, 64))])
+        cpu = cpu_baseline_of(first["w"], shape, xin, args.cpu_seconds, 200,
+                              f"layer 0 of the stack on its first layer inputs; tokens/s through {L} layers "
+                              "= the per-layer rate / the layer count", per_token_factor=L)
     lookups = max(d["hits"] + d["misses"], 1)
     print(json.dumps({
         "metric": metric_of(shape),
@@ -466,6 +528,7 @@ def run_stack(args, shape):
         "roofline": {"bound": "pcie", "achieved": d["bytes_filled"] / (ms * 1e-3) / 1e9,
                      "peak": h2d_gbs, "unit": "GB/s", "frac": d["bytes_filled"] / (ms * 1e-3) / 1e9 / h2d_gbs,
                      "traffic": None, "peak_kind": "measured in this run: 64 pinned blob copies"},
+        "cpu_baseline": cpu,
         "clocks": clk.summary(), "wall_s": t_wall,
     }), flush=True)
     st.close()
@@ -551,7 +614,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="80b-dec",
-                    choices=["80b-dec", "35b-dec", "80b-prefill", "80b-stack", "policy-study"])
+                    choices=["80b-dec", "35b-dec", "80b-dec-int8", "35b-dec-int8", "80b-prefill", "80b-stack",
+                             "policy-study"])
     ap.add_argument("--tokens", type=int, default=1000, help="decode tokens per bench step")
     ap.add_argument("--replicas", type=int, default=0, help="layer copies to rotate through (0 = >= 3x L2)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -659,6 +723,25 @@ def main():
         torch.cuda.synchronize()
     e2e_value = job_tokens_per_s(e2e_steps * T, world, max_over_ranks(e0.elapsed_time(e1), dist, "cuda"))
 
+    # ---- the same tokens through one copy of the layer (no rotation): the
+    # router, the shared expert and repeatedly chosen experts can stay in L2
+    graph1 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph1, stream=stream):
+        for j in range(T):
+            B.moe_layer_forward(cfg, dl.struct(0), xs[j:j + 1], 1, ys[j:j + 1], None, None, None, ws, nb)
+    steps1 = max(1, min(args.steps, 20))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            graph1.replay()
+        n0, n1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n0.record(stream)
+        for _ in range(steps1):
+            graph1.replay()
+        n1.record(stream)
+    torch.cuda.synchronize()
+    nr_us = n0.elapsed_time(n1) * 1e3 / (steps1 * T)
+    del graph1
+
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -676,17 +759,15 @@ def main():
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:  # the oracle's baseline is an N = 1 figure
-        v, n, dt = oracle_tokens_per_s(w, shape, xs, args.cpu_seconds, 400)
-        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"first {n} of the {T} seeded decode tokens of one bench step ({dt:.1f} s, "
-                         "single-threaded C, fp64)"}
+        cpu = cpu_baseline_of(w, shape, xs, args.cpu_seconds, 400,
+                              f"first tokens of the {T} seeded decode tokens of one bench step")
 
     line = {
         "metric": metric_of(shape), "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "s32/f32", "data": "synthetic",
-        "dtype_note": "int4 codes x 16-bit fixed-point activations in dp4a (s32), group scales and sums in f32; "
-                      "bf16 x in, bf16 y out",
+        "dtype_note": f"int{shape.bits} codes x 16-bit fixed-point activations in dp4a (s32), group scales and "
+                      "sums in f32; bf16 x in, bf16 y out",
         "config": {"workload": workload_desc(shape), "tokens_per_step": T, "parallelism": f"replicas{world}",
                    "l2": f"inputs larger than L2: tokens rotate through {R} full layer copies "
                          f"({R * dl.stride * dl.n_slots / 1e9:.1f} GB; the weights {R} tokens touch are "
@@ -702,6 +783,10 @@ def main():
                      "frac": achieved / peak, "traffic": traffic, "mean_us": mean_us,
                      "algorithmic_bytes_per_launch": per_token},
         "cpu_baseline": cpu,
+        "non_rotated": {"tokens_per_s": job_tokens_per_s(T, world, nr_us * T / 1e3), "us_per_call": nr_us,
+                        "achieved_gbs": per_token / (nr_us * 1e-6) / 1e9,
+                        "note": "one layer copy for every token: weights that repeat across tokens (router, "
+                                "shared expert, experts chosen again) may come from L2; not a roofline figure"},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": x_host.numel() * 2,
                 "d2h_bytes_per_step": y_host.numel() * 2,
                 "how": "per step: one pinned H2D of the step's x, moe_layer_forward per token (eager, "

@@ -56,7 +56,10 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_F16 = 2 } moe_dtype;
  *   multiples of 32; E <= 1024).
  *   act_dtype: x and y, MOE_F32 or MOE_BF16.
  *   router_dtype: router and shared-gate weights, MOE_F32 or MOE_BF16.
- *   qscale_dtype: per-group scale and bias, MOE_F32 or MOE_F16. */
+ *   qscale_dtype: per-group scale and bias, MOE_F32 or MOE_F16.
+ *   bits: code width of the expert weights, 4 or 8 (MLX affine int4 or
+ *   int8 group quantisation, page 2 "Relation to TurboFieldfare"); 0 means
+ *   4, so a zero-initialised field keeps the int4 layout. */
 typedef struct {
     int32_t hidden;
     int32_t n_experts;
@@ -67,13 +70,14 @@ typedef struct {
     int32_t act_dtype;
     int32_t router_dtype;
     int32_t qscale_dtype;
+    int32_t bits;
 } moe_config;
 
-/* One affine int4 matrix W [out, in] (MLX layout): q is uint32 [out, in/8]
- * with column c of row o in word [o, c/8] at bits 4*(c%8)..4*(c%8)+3 (lowest
- * column in the lowest nibble); scale and bias are [out, in/G] in
- * qscale_dtype; W[o,c] = scale[o,c/G] * q + bias[o,c/G].  q must be 16-byte
- * aligned. */
+/* One affine matrix W [out, in] (MLX layout) with b-bit codes (b = bits, 4
+ * or 8): q is uint32 [out, in*b/32] with column c of row o in word
+ * [o, c*b/32] at bits b*(c%(32/b)) .. b*(c%(32/b))+b-1 (lowest column in the
+ * lowest bits); scale and bias are [out, in/G] in qscale_dtype;
+ * W[o,c] = scale[o,c/G] * q + bias[o,c/G].  q must be 16-byte aligned. */
 typedef struct {
     const uint32_t *q;
     const void *scale;

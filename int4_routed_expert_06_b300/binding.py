@@ -40,7 +40,7 @@ class MoEError(RuntimeError):
 
 class moe_config(C.Structure):
     _fields_ = [(n, C.c_int32) for n in ("hidden", "n_experts", "top_k", "inter", "shared_inter",
-                                         "group_size", "act_dtype", "router_dtype", "qscale_dtype")]
+                                         "group_size", "act_dtype", "router_dtype", "qscale_dtype", "bits")]
 
 
 class moe_qmat(C.Structure):
@@ -317,7 +317,7 @@ def moe_debug_set_waits(wait_ns: int, extra_arrivals: int) -> None:
 def config_for(shape) -> moe_config:
     """moe_config of a synth.MoEShape."""
     return moe_config(shape.hidden, shape.n_experts, shape.top_k, shape.inter, shape.shared_inter, shape.group,
-                      _DTYPE[shape.act], _DTYPE[shape.router], _DTYPE[shape.qscale])
+                      _DTYPE[shape.act], _DTYPE[shape.router], _DTYPE[shape.qscale], getattr(shape, "bits", 4))
 
 
 _ARRAYS = ("q_gate", "q_up", "q_down", "s_gate", "b_gate", "s_up", "b_up", "s_down", "b_down")

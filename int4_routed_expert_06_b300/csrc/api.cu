@@ -63,6 +63,8 @@ moe_status check_config(const moe_config *c, Shape *s)
         return fail(MOE_ERR_UNSUPPORTED, "router_dtype must be MOE_F32 or MOE_BF16");
     if (c->qscale_dtype != MOE_F32 && c->qscale_dtype != MOE_F16)
         return fail(MOE_ERR_UNSUPPORTED, "qscale_dtype must be MOE_F32 or MOE_F16");
+    if (c->bits != 0 && c->bits != 4 && c->bits != 8)
+        return fail(MOE_ERR_UNSUPPORTED, "bits %d: 4 or 8 supported (0 means 4)", c->bits);
     if (s) {
         s->H = c->hidden;
         s->E = c->n_experts;
@@ -73,6 +75,7 @@ moe_status check_config(const moe_config *c, Shape *s)
         s->act = c->act_dtype;
         s->router = c->router_dtype;
         s->qscale = c->qscale_dtype;
+        s->bits = c->bits == 8 ? 8 : 4;
     }
     return MOE_OK;
 }
@@ -96,7 +99,7 @@ static Ws layer_ws(const Shape &s, int T)
     w.tok = o;    o += T == 1 ? align256(tok::bufs_bytes(s)) : 0;
     w.hist = o;   o += align256(sizeof(int32_t) * (size_t)bucket_chunks(T * s.k) * s.E);
     w.pre = o;
-    if (T >= prefill::kMinTokens && s.H % 128 == 0 && s.I % 64 == 0 && s.Is % 64 == 0 && s.Is > 0)
+    if (T >= prefill::kMinTokens && s.bits == 4 && s.H % 128 == 0 && s.I % 64 == 0 && s.Is % 64 == 0 && s.Is > 0)
         o += align256(prefill::layout(s, T).total);
     w.total = o;
     return w;
@@ -138,7 +141,7 @@ moe_status moe_blob_layout_get(const moe_config *cfg, int32_t inter, moe_blob_la
     if (inter <= 0 || inter % 32 || inter % s.G)
         return fail(MOE_ERR_INVALID_ARG, "moe_blob_layout_get: inter %d", inter);
     const size_t sb = scale_bytes(s.qscale);
-    const size_t qgu = (size_t)inter * s.H / 2, qd = (size_t)s.H * inter / 2;
+    const size_t qgu = (size_t)inter * s.H * s.bits / 8, qd = (size_t)s.H * inter * s.bits / 8;
     const size_t sgu = (size_t)inter * (s.H / s.G) * sb, sd = (size_t)s.H * (inter / s.G) * sb;
     size_t o = 0;
     out->q_gate = o; o = align256(o + qgu);
@@ -167,7 +170,8 @@ moe_status moe_pack_expert(const moe_config *cfg, int32_t inter, const moe_exper
         if (!m[j]->q || !m[j]->scale || !m[j]->bias)
             return fail(MOE_ERR_INVALID_ARG, "moe_pack_expert: NULL array in matrix %d", j);
     const size_t sb = scale_bytes(cfg->qscale_dtype);
-    const size_t qgu = (size_t)inter * cfg->hidden / 2, qd = (size_t)cfg->hidden * inter / 2;
+    const int bits = cfg->bits == 8 ? 8 : 4;
+    const size_t qgu = (size_t)inter * cfg->hidden * bits / 8, qd = (size_t)cfg->hidden * inter * bits / 8;
     const size_t sgu = (size_t)inter * (cfg->hidden / cfg->group_size) * sb;
     const size_t sd = (size_t)cfg->hidden * (inter / cfg->group_size) * sb;
     char *d = static_cast<char *>(dst);

@@ -13,6 +13,7 @@ namespace moe {
 struct Shape {
     int H, E, k, I, Is, G;
     int act, router, qscale; // moe_dtype values
+    int bits;                // code width: 4 or 8
 };
 
 // Record a thread-local message and return `st`.

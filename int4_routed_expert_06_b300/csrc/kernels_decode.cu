@@ -1,4 +1,5 @@
-// Router, top-k and the decode-path expert kernels of the routed int4 MoE layer.
+// Router, top-k and the generic expert kernels of the routed MoE layer
+// (affine int4 or int8 codes).
 //
 // Decode is bandwidth-bound: every active expert's packed weights are read
 // once per token, so the kernels stream them with 16-byte loads and do the
@@ -191,8 +192,9 @@ cudaError_t launch_topk(const Shape &s, const float *logits, int T, int32_t *idx
 // distinct banks within each 8-lane phase.
 __host__ __device__ __forceinline__ int padded(int c) { return c + (c >> 5) * 4; }
 
-// Dot of one 16-byte chunk of codes (32 columns, all in one quantisation
-// group) with 32 fp32 values at v (padded layout, 16-byte aligned).
+// Dot of one chunk of codes (32 columns, all in one quantisation group) with
+// 32 fp32 values at v (padded layout, 16-byte aligned).  BITS = 4: the
+// chunk's codes are one 16-byte word q; BITS = 8: two, q then q2.
 __device__ __forceinline__ float chunk_code_dot(uint4 q, const float *v)
 {
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
@@ -213,10 +215,40 @@ __device__ __forceinline__ float chunk_code_dot(uint4 q, const float *v)
     return acc;
 }
 
+// 8-bit code j (byte j) of a word -> exact fp32.
+__device__ __forceinline__ float code8_f32(uint32_t word, int j)
+{
+    return __uint_as_float(((word >> (8 * j)) & 0xFFu) | 0x4B000000u) - 8388608.0f;
+}
+
+__device__ __forceinline__ float chunk_code_dot8(uint4 q, uint4 q2, const float *v)
+{
+    const uint32_t w[8] = {q.x, q.y, q.z, q.w, q2.x, q2.y, q2.z, q2.w};
+    float acc = 0.f;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        const float4 v0 = *reinterpret_cast<const float4 *>(v + 4 * m);
+        acc = fmaf(code8_f32(w[m], 0), v0.x, acc);
+        acc = fmaf(code8_f32(w[m], 1), v0.y, acc);
+        acc = fmaf(code8_f32(w[m], 2), v0.z, acc);
+        acc = fmaf(code8_f32(w[m], 3), v0.w, acc);
+    }
+    return acc;
+}
+
+// The code dot of chunk ch of a row whose words start at q (BITS-bit codes).
+template <int BITS>
+__device__ __forceinline__ float row_chunk_dot(const uint4 *q, int ch, const float *v)
+{
+    if (BITS == 8)
+        return chunk_code_dot8(__ldg(q + 2 * ch), __ldg(q + 2 * ch + 1), v);
+    return chunk_code_dot(__ldg(q + ch), v);
+}
+
 // Gate/up + SwiGLU, one warp per output row o of active expert i of token t:
 //   a[t, i, o] = silu(g) * u,  g = W_g[o] . x[t],  u = W_u[o] . x[t].
 // grid: (ceil(Imax / 8), n_act, T); 256 threads.
-template <typename TA, typename TS>
+template <typename TA, typename TS, int BITS>
 __global__ void __launch_bounds__(256) gateup_kernel(const TA *__restrict__ x, int H, int G, int k,
                                                      int n_act, int I, int Is,
                                                      const int32_t *__restrict__ topk_idx,
@@ -252,7 +284,7 @@ __global__ void __launch_bounds__(256) gateup_kernel(const TA *__restrict__ x, i
             *dst = 0.f;
         return;
     }
-    const int wpr = H >> 3, gpr = H / G;
+    const int wpr = H * BITS / 32, gpr = H / G;
     const uint4 *qg = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint32_t *>(p[M_QG]) + (size_t)o * wpr);
     const uint4 *qu = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint32_t *>(p[M_QU]) + (size_t)o * wpr);
     const TS *sg = reinterpret_cast<const TS *>(p[M_SG]) + (size_t)o * gpr;
@@ -261,12 +293,10 @@ __global__ void __launch_bounds__(256) gateup_kernel(const TA *__restrict__ x, i
     const TS *bu = reinterpret_cast<const TS *>(p[M_BU]) + (size_t)o * gpr;
     float gacc = 0.f, uacc = 0.f;
     for (int ch = lane; ch < nch; ch += 32) {
-        const uint4 wg = __ldg(qg + ch);
-        const uint4 wu = __ldg(qu + ch);
         const int grp = (ch * 32) / G;
         const float *v = xs + ch * 36;
-        const float dg = chunk_code_dot(wg, v);
-        const float du = chunk_code_dot(wu, v);
+        const float dg = row_chunk_dot<BITS>(qg, ch, v);
+        const float du = row_chunk_dot<BITS>(qu, ch, v);
         const float xsm = xsum[ch];
         gacc += to_f32(sg[grp]) * dg + to_f32(bg[grp]) * xsm;
         uacc += to_f32(su[grp]) * du + to_f32(bu[grp]) * xsm;
@@ -277,7 +307,7 @@ __global__ void __launch_bounds__(256) gateup_kernel(const TA *__restrict__ x, i
         *dst = g * sigmoid_f(g) * u;
 }
 
-template <typename TS>
+template <typename TS, int BITS>
 static cudaError_t gateup_dispatch(const Shape &s, const void *x, int T, int k_eff, int n_act,
                                    const int32_t *idx, const ExpertSrc &src, float *a, int Imax,
                                    cudaStream_t st)
@@ -285,14 +315,14 @@ static cudaError_t gateup_dispatch(const Shape &s, const void *x, int T, int k_e
     dim3 grid((Imax + 7) / 8, n_act, T);
     size_t smem = (size_t)(s.H + s.H / 8 + s.H / 32) * sizeof(float);
     if (s.act == MOE_BF16) {
-        auto kern = gateup_kernel<__nv_bfloat16, TS>;
+        auto kern = gateup_kernel<__nv_bfloat16, TS, BITS>;
         static int cur_smem = 0;
         cudaError_t e = ensure_smem(kern, smem, &cur_smem);
         if (e != cudaSuccess)
             return e;
         kern<<<grid, 256, smem, st>>>((const __nv_bfloat16 *)x, s.H, s.G, k_eff, n_act, s.I, s.Is, idx, src, a, Imax);
     } else {
-        auto kern = gateup_kernel<float, TS>;
+        auto kern = gateup_kernel<float, TS, BITS>;
         static int cur_smem = 0;
         cudaError_t e = ensure_smem(kern, smem, &cur_smem);
         if (e != cudaSuccess)
@@ -306,9 +336,12 @@ cudaError_t launch_gateup(const Shape &s, const void *x, int T, int k_eff, int n
                           const int32_t *topk_idx, const ExpertSrc &src, float *a, int Imax,
                           cudaStream_t st)
 {
+    if (s.bits == 8)
+        return s.qscale == MOE_F16 ? gateup_dispatch<__half, 8>(s, x, T, k_eff, n_act, topk_idx, src, a, Imax, st)
+                                   : gateup_dispatch<float, 8>(s, x, T, k_eff, n_act, topk_idx, src, a, Imax, st);
     if (s.qscale == MOE_F16)
-        return gateup_dispatch<__half>(s, x, T, k_eff, n_act, topk_idx, src, a, Imax, st);
-    return gateup_dispatch<float>(s, x, T, k_eff, n_act, topk_idx, src, a, Imax, st);
+        return gateup_dispatch<__half, 4>(s, x, T, k_eff, n_act, topk_idx, src, a, Imax, st);
+    return gateup_dispatch<float, 4>(s, x, T, k_eff, n_act, topk_idx, src, a, Imax, st);
 }
 
 // Down projection + weighted combine.  A warp owns two output rows; each
@@ -318,7 +351,7 @@ cudaError_t launch_gateup(const Shape &s, const void *x, int T, int k_eff, int n
 //   y[t, h] = sum_{r<k} w[t,r] dot_r + sigmoid(gate_logit[t]) dot_shared.
 // topk_w == NULL means weight 1; gate_logit == NULL means shared weight 1.
 // grid: (H / 16, T); 256 threads.
-template <typename TA, typename TS>
+template <typename TA, typename TS, int BITS>
 __global__ void __launch_bounds__(256) down_kernel(const float *__restrict__ a, int H, int G, int k,
                                                    int n_act, int I, int Is, int Imax,
                                                    const int32_t *__restrict__ topk_idx,
@@ -364,14 +397,13 @@ __global__ void __launch_bounds__(256) down_kernel(const float *__restrict__ a, 
         const char *const *p = bases + i * 9;
         float dot = 0.f;
         if (p[M_QD] != nullptr && h < H) {
-            const int wpr = inter >> 3, gpr = inter / G, nch = inter >> 5;
+            const int wpr = inter * BITS / 32, gpr = inter / G, nch = inter >> 5;
             const uint4 *qd = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint32_t *>(p[M_QD]) + (size_t)h * wpr);
             const TS *sd = reinterpret_cast<const TS *>(p[M_SD]) + (size_t)h * gpr;
             const TS *bd = reinterpret_cast<const TS *>(p[M_BD]) + (size_t)h * gpr;
             for (int ch = l16; ch < nch; ch += 16) {
-                const uint4 wq = __ldg(qd + ch);
                 const int grp = (ch * 32) / G;
-                const float d = chunk_code_dot(wq, as + i * pI + ch * 36);
+                const float d = row_chunk_dot<BITS>(qd, ch, as + i * pI + ch * 36);
                 dot += to_f32(sd[grp]) * d + to_f32(bd[grp]) * asum[i * nchm + ch];
             }
         }
@@ -390,7 +422,7 @@ __global__ void __launch_bounds__(256) down_kernel(const float *__restrict__ a, 
     }
 }
 
-template <typename TS>
+template <typename TS, int BITS>
 static cudaError_t down_dispatch(const Shape &s, const float *a, int T, int k_eff, int n_act,
                                  int Imax, const int32_t *idx, const float *w, const float *gl,
                                  const ExpertSrc &src, void *y, float *y32, cudaStream_t st)
@@ -398,7 +430,7 @@ static cudaError_t down_dispatch(const Shape &s, const float *a, int T, int k_ef
     dim3 grid((s.H + 15) / 16, T);
     size_t smem = (size_t)(((n_act * 9 * 2 + 3) & ~3) + n_act * (padded(Imax) + Imax / 32)) * sizeof(float);
     if (s.act == MOE_BF16) {
-        auto kern = down_kernel<__nv_bfloat16, TS>;
+        auto kern = down_kernel<__nv_bfloat16, TS, BITS>;
         static int cur_smem = 0;
         cudaError_t e = ensure_smem(kern, smem, &cur_smem);
         if (e != cudaSuccess)
@@ -406,7 +438,7 @@ static cudaError_t down_dispatch(const Shape &s, const float *a, int T, int k_ef
         kern<<<grid, 256, smem, st>>>(a, s.H, s.G, k_eff, n_act, s.I, s.Is, Imax, idx, w, gl, src,
                                       (__nv_bfloat16 *)y, y32);
     } else {
-        auto kern = down_kernel<float, TS>;
+        auto kern = down_kernel<float, TS, BITS>;
         static int cur_smem = 0;
         cudaError_t e = ensure_smem(kern, smem, &cur_smem);
         if (e != cudaSuccess)
@@ -421,9 +453,13 @@ cudaError_t launch_down(const Shape &s, const float *a, int T, int k_eff, int n_
                         const int32_t *topk_idx, const float *topk_w, const float *gate_logit,
                         const ExpertSrc &src, void *y, float *y32, cudaStream_t st)
 {
+    if (s.bits == 8)
+        return s.qscale == MOE_F16
+                   ? down_dispatch<__half, 8>(s, a, T, k_eff, n_act, Imax, topk_idx, topk_w, gate_logit, src, y, y32, st)
+                   : down_dispatch<float, 8>(s, a, T, k_eff, n_act, Imax, topk_idx, topk_w, gate_logit, src, y, y32, st);
     if (s.qscale == MOE_F16)
-        return down_dispatch<__half>(s, a, T, k_eff, n_act, Imax, topk_idx, topk_w, gate_logit, src, y, y32, st);
-    return down_dispatch<float>(s, a, T, k_eff, n_act, Imax, topk_idx, topk_w, gate_logit, src, y, y32, st);
+        return down_dispatch<__half, 4>(s, a, T, k_eff, n_act, Imax, topk_idx, topk_w, gate_logit, src, y, y32, st);
+    return down_dispatch<float, 4>(s, a, T, k_eff, n_act, Imax, topk_idx, topk_w, gate_logit, src, y, y32, st);
 }
 
 } // namespace moe

@@ -265,6 +265,46 @@ __device__ __forceinline__ float chunk_term(uint4 q, const Chunk &c, float s, fl
     return fmaf(s, D, b * c.X);
 }
 
+// 8-bit codes of columns 8m..8m+7 (word w0: columns 8m..8m+3, w1: 8m+4..8m+7)
+// in the record order: byte j of ev is column 8m+2j, of od column 8m+2j+1.
+__device__ __forceinline__ void split8(uint32_t w0, uint32_t w1, uint32_t &ev, uint32_t &od)
+{
+    ev = __byte_perm(w0, w1, 0x6420);
+    od = __byte_perm(w0, w1, 0x7531);
+}
+
+// chunk_idot for 8-bit codes: the chunk's 32 codes are the two words qa, qb
+// (columns 0..15, 16..31).  Exact: |sum| < 2^29.
+__device__ __forceinline__ int chunk_idot8(uint4 qa, uint4 qb, const Chunk &c)
+{
+    const uint32_t w[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+    const uint32_t he[4] = {c.he.x, c.he.y, c.he.z, c.he.w};
+    const uint32_t le[4] = {c.le.x, c.le.y, c.le.z, c.le.w};
+    const uint32_t ho[4] = {c.ho.x, c.ho.y, c.ho.z, c.ho.w};
+    const uint32_t lo[4] = {c.lo.x, c.lo.y, c.lo.z, c.lo.w};
+    int h0 = 0, h1 = 0, l0 = 0, l1 = 0;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        uint32_t ev, od;
+        split8(w[2 * m], w[2 * m + 1], ev, od);
+        h0 = dp4a_us(ev, he[m], h0);
+        h1 = dp4a_us(od, ho[m], h1);
+        l0 = dp4a_uu(ev, le[m], l0);
+        l1 = dp4a_uu(od, lo[m], l1);
+    }
+    return (h0 + h1) * 256 + (l0 + l1);
+}
+
+// The codes of chunk ch of a BITS-bit code row at row (shared memory), as a
+// chunk term.
+template <int BITS>
+__device__ __forceinline__ float row_chunk_term(const unsigned char *row, int ch, const Chunk &c, float s, float b)
+{
+    const uint4 *q = reinterpret_cast<const uint4 *>(row);
+    const int D = BITS == 8 ? chunk_idot8(q[2 * ch], q[2 * ch + 1], c) : chunk_idot(q[ch], c);
+    return fmaf(s, (float)D * c.sx, b * c.X);
+}
+
 // ------------------------------------------------------------ top-k
 
 // 32-bit order key of a logit: unsigned order = float order, NaN as -inf;
@@ -568,10 +608,11 @@ __device__ __forceinline__ void named_sync(int id, int nthreads)
 // x 56) beside it, each of the SM's four register banks holds its share of
 // all three kernels, so each kernel's CTAs are resident before its
 // predecessor ends.
-template <int NXC, typename TS>
+template <int NXC, typename TS, int BITS>
 __global__ void __maxnreg__(72) gateup_tok_kernel(TokArgs A)
 {
     constexpr int H = 1024 * NXC;
+    constexpr uint32_t RB = H * BITS / 8; // bytes of one code row
     constexpr int NG = kGuWarps / 4; // warp groups
     constexpr int kDepth = 3;        // routed units in flight
     extern __shared__ __align__(128) unsigned char units[]; // [local unit][unitb]
@@ -591,7 +632,7 @@ __global__ void __maxnreg__(72) gateup_tok_kernel(TokArgs A)
     const int js = max(0, min(nu, (A.Is >> 3) - u0)); // local units [0, js) are the shared expert's
     const int HG = H >> A.log2G;
     const uint32_t sbr = (uint32_t)HG * (uint32_t)sizeof(TS); // bytes of one scale row
-    const uint32_t unitb = 8u * ((uint32_t)H + 4u * sbr);
+    const uint32_t unitb = 8u * (2u * RB + 4u * sbr);
 
     // The copies of local unit j, by one warp: lane a < 6 copies array a
     // (gate codes, up codes, gate scales, gate biases, up scales, up biases)
@@ -607,10 +648,9 @@ __global__ void __maxnreg__(72) gateup_tok_kernel(TokArgs A)
             const size_t *offs = i == k ? A.src.off_sh : A.src.off;
             unsigned char *d = units + (size_t)j * unitb;
             if (lane < 2)
-                bulk_g2s(d + lane * 8 * (H / 2), b + offs[lane ? M_QU : M_QG] + (size_t)o0 * (H / 2), 8u * (H / 2),
-                         &ubar[j]);
+                bulk_g2s(d + lane * 8 * RB, b + offs[lane ? M_QU : M_QG] + (size_t)o0 * RB, 8u * RB, &ubar[j]);
             else
-                bulk_g2s(d + 8 * H + (lane - 2) * 8 * sbr, b + offs[M_SG + (lane - 2)] + (size_t)o0 * sbr, 8u * sbr,
+                bulk_g2s(d + 16 * RB + (lane - 2) * 8 * sbr, b + offs[M_SG + (lane - 2)] + (size_t)o0 * sbr, 8u * sbr,
                          &ubar[j]);
         }
     };
@@ -665,7 +705,7 @@ __global__ void __maxnreg__(72) gateup_tok_kernel(TokArgs A)
         if (wq == 0 && j >= js && j + kDepth < nu)
             stage(j + kDepth);
         const unsigned char *d = units + (size_t)j * unitb;
-        const TS *sc = reinterpret_cast<const TS *>(d + 8 * H);
+        const TS *sc = reinterpret_cast<const TS *>(d + 16 * RB);
         float v[4] = {0.f, 0.f, 0.f, 0.f}; // gate, up of rows 2 wq and 2 wq + 1
         if (have) {
 #pragma unroll
@@ -675,11 +715,10 @@ __global__ void __maxnreg__(72) gateup_tok_kernel(TokArgs A)
                 for (int m = 0; m < NXC; ++m) {
                     const int ch = lane + 32 * m;
                     const int gi = (ch * 32) >> A.log2G;
-                    const uint4 qg = reinterpret_cast<const uint4 *>(d + r * (H / 2))[ch];
-                    const uint4 qu = reinterpret_cast<const uint4 *>(d + 8 * (H / 2) + r * (H / 2))[ch];
-                    v[2 * rr] += chunk_term(qg, xv[m], to_f32(sc[r * HG + gi]), to_f32(sc[8 * HG + r * HG + gi]));
-                    v[2 * rr + 1] +=
-                        chunk_term(qu, xv[m], to_f32(sc[16 * HG + r * HG + gi]), to_f32(sc[24 * HG + r * HG + gi]));
+                    v[2 * rr] += row_chunk_term<BITS>(d + r * RB, ch, xv[m], to_f32(sc[r * HG + gi]),
+                                                      to_f32(sc[8 * HG + r * HG + gi]));
+                    v[2 * rr + 1] += row_chunk_term<BITS>(d + (8 + r) * RB, ch, xv[m], to_f32(sc[16 * HG + r * HG + gi]),
+                                                          to_f32(sc[24 * HG + r * HG + gi]));
                 }
             }
         }
@@ -758,6 +797,26 @@ __device__ __forceinline__ float arec_term(uint4 q, uint4 he, uint4 le, uint4 ho
     return fmaf(s, D, b * ((X.x + X.y) + (X.z + X.w)));
 }
 
+// arec_term for 8-bit codes: the chunk's 32 codes are the words qa, qb.
+__device__ __forceinline__ float arec_term8(uint4 qa, uint4 qb, uint4 he, uint4 le, uint4 ho, uint4 lo, float4 sx,
+                                            float4 X, float s, float b)
+{
+    const uint32_t w[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+    const uint32_t H_[4] = {he.x, he.y, he.z, he.w}, L_[4] = {le.x, le.y, le.z, le.w};
+    const uint32_t HO[4] = {ho.x, ho.y, ho.z, ho.w}, LO[4] = {lo.x, lo.y, lo.z, lo.w};
+    const float S[4] = {sx.x, sx.y, sx.z, sx.w};
+    float D = 0.f;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        uint32_t ev, od;
+        split8(w[2 * m], w[2 * m + 1], ev, od);
+        const int h = dp4a_us(od, HO[m], dp4a_us(ev, H_[m], 0));
+        const int l = dp4a_uu(od, LO[m], dp4a_uu(ev, L_[m], 0));
+        D = fmaf((float)(h * 256 + l), S[m], D);
+    }
+    return fmaf(s, D, b * ((X.x + X.y) + (X.z + X.w)));
+}
+
 // Down projection and combine.  CTA c computes output rows [h0, h1) =
 // [c H / n, (c + 1) H / n).  Its W_d rows of every active expert (codes
 // [nr][I_i/2], then scales and biases [nr][I_i/G] each, per expert) are bulk-
@@ -770,7 +829,7 @@ __device__ __forceinline__ float arec_term(uint4 q, uint4 he, uint4 le, uint4 ho
 // adds its half's warps in order: a fixed summation order, so the result does
 // not depend on where the experts live.  The routing (with weights) is
 // computed before the wait.
-template <typename TS>
+template <typename TS, int BITS>
 __global__ void __maxnreg__(56) down_tok_kernel(TokArgs A, int H)
 {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -799,7 +858,7 @@ __global__ void __maxnreg__(56) down_tok_kernel(TokArgs A, int H)
         for (int i = 0; i < n_act; ++i) {
             const int inter = i == k ? A.Is : A.I;
             s_eoff[i] = off;
-            off += (uint32_t)nr * ((uint32_t)inter / 2 + 2 * (uint32_t)(inter >> A.log2G) * sb);
+            off += (uint32_t)nr * ((uint32_t)inter * BITS / 8 + 2 * (uint32_t)(inter >> A.log2G) * sb);
         }
         s_eoff[n_act] = off;
         s_base[k] = A.src.shared;
@@ -820,7 +879,7 @@ __global__ void __maxnreg__(56) down_tok_kernel(TokArgs A, int H)
     if (warp == 0) {
         const char *b = lane < n_act ? s_base[lane] : nullptr;
         const int inter = lane == k ? A.Is : A.I;
-        const uint32_t qb = (uint32_t)inter / 2, sbb = (uint32_t)(inter >> A.log2G) * sb;
+        const uint32_t qb = (uint32_t)inter * BITS / 8, sbb = (uint32_t)(inter >> A.log2G) * sb;
         const uint32_t nq = b ? (uint32_t)nr * qb : 0u, nsb = b ? (uint32_t)nr * sbb : 0u;
         const uint32_t tot = __reduce_add_sync(0xFFFFFFFFu, nq + 2 * nsb);
         if (lane == 0)
@@ -883,7 +942,7 @@ __global__ void __maxnreg__(56) down_tok_kernel(TokArgs A, int H)
             const float4 X = make_float4(__uint_as_float(Xu.x), __uint_as_float(Xu.y), __uint_as_float(Xu.z),
                                          __uint_as_float(Xu.w));
             const int inter = i == k ? A.Is : A.I;
-            const int qb = inter / 2, ng = inter >> A.log2G;
+            const int qb = inter * BITS / 8, ng = inter >> A.log2G;
             const unsigned char *d = down + s_eoff[i];
             const TS *sd = reinterpret_cast<const TS *>(d + nr * qb);
             const TS *bd = sd + nr * ng;
@@ -894,9 +953,10 @@ __global__ void __maxnreg__(56) down_tok_kernel(TokArgs A, int H)
 #pragma unroll
             for (int rr = 0; rr < kMaxRH; ++rr) {
                 const int r = r0 + min(rr, nrr - 1);
-                const uint4 q = reinterpret_cast<const uint4 *>(d + r * qb)[ch];
-                const float term =
-                    wi * arec_term(q, he, le, ho, lo, sx, X, to_f32(sd[r * ng + g]), to_f32(bd[r * ng + g]));
+                const uint4 *q = reinterpret_cast<const uint4 *>(d + r * qb);
+                const float s = to_f32(sd[r * ng + g]), b = to_f32(bd[r * ng + g]);
+                const float term = wi * (BITS == 8 ? arec_term8(q[2 * ch], q[2 * ch + 1], he, le, ho, lo, sx, X, s, b)
+                                                   : arec_term(q[ch], he, le, ho, lo, sx, X, s, b));
                 v[rr] = rr < nrr ? term : 0.f;
             }
         }
@@ -978,7 +1038,7 @@ static size_t down_smem(const Shape &s, int n)
     size_t w = 0;
     for (int i = 0; i <= s.k; ++i) {
         const int inter = (i == s.k) ? s.Is : s.I;
-        w += (size_t)nr * (inter / 2 + 2 * (inter / s.G) * sb);
+        w += (size_t)nr * ((size_t)inter * s.bits / 8 + 2 * (inter / s.G) * sb);
     }
     w = (w + 127) & ~(size_t)127;
     return w + (size_t)kArec * n_chunks(s);
@@ -989,19 +1049,22 @@ static size_t down_smem(const Shape &s, int n)
 static size_t gateup_smem(const Shape &s, int n)
 {
     const size_t sb = s.qscale == MOE_F16 ? 2 : 4;
-    const size_t unitb = 8 * ((size_t)s.H + 4 * (size_t)(s.H / s.G) * sb);
+    const size_t unitb = 8 * (2 * (size_t)s.H * s.bits / 8 + 4 * (size_t)(s.H / s.G) * sb);
     return (size_t)((n_units(s) + n - 1) / n) * unitb;
 }
 
-// The gate/up and down kernels share an SM (with their static arrays, within
-// its 228 KB).
+// With 4-bit codes the gate/up and down kernels share an SM (with their
+// static arrays, within its 228 KB).  With 8-bit codes each fits alone: a down
+// CTA then starts on an SM as its gate/up CTA ends (nothing waits on their
+// being resident together).
 constexpr size_t kSmemLimit = 196 * 1024;
+constexpr size_t kSmemLimitAlone = 200 * 1024;
 
 bool eligible(const Shape &s)
 {
     if (kernel_path() != 0)
         return false;
-    if (s.act != MOE_BF16 || s.router != MOE_BF16)
+    if (s.act != MOE_BF16 || s.router != MOE_BF16 || (s.bits != 4 && s.bits != 8))
         return false;
     if (s.H != 1024 && s.H != 2048)
         return false;
@@ -1018,6 +1081,8 @@ bool eligible(const Shape &s)
     // down: two threads (row halves) to each chunk, rounded up to whole warps
     if (2 * ((n_chunks(s) + 31) & ~31) > kDnThreads || (s.H + n - 1) / n > 2 * kMaxRH)
         return false;
+    if (s.bits == 8)
+        return gateup_smem(s, n) <= kSmemLimitAlone && down_smem(s, n) <= kSmemLimitAlone;
     return gateup_smem(s, n) + down_smem(s, n) <= kSmemLimit;
 }
 
@@ -1085,23 +1150,34 @@ cudaError_t launch_router(const Shape &s, const void *x, const void *w_router, c
                                          sg, xrec, xrs, row_ctas);
 }
 
-template <int NXC, typename TS>
+template <int NXC, typename TS, int BITS>
 static cudaError_t experts_go(const TokArgs &A, int n, size_t gsmem, size_t smem, int H, cudaStream_t st)
 {
     static int cur = 0, gcur = 0;
     static bool cvg = false, cvd = false;
-    cudaError_t e = set_carveout(gateup_tok_kernel<NXC, TS>, &cvg);
+    cudaError_t e = set_carveout(gateup_tok_kernel<NXC, TS, BITS>, &cvg);
     if (e == cudaSuccess)
-        e = set_carveout(down_tok_kernel<TS>, &cvd);
+        e = set_carveout(down_tok_kernel<TS, BITS>, &cvd);
     if (e == cudaSuccess)
-        e = ensure_smem(down_tok_kernel<TS>, smem, &cur);
+        e = ensure_smem(down_tok_kernel<TS, BITS>, smem, &cur);
     if (e == cudaSuccess)
-        e = ensure_smem(gateup_tok_kernel<NXC, TS>, gsmem, &gcur);
+        e = ensure_smem(gateup_tok_kernel<NXC, TS, BITS>, gsmem, &gcur);
     if (e == cudaSuccess)
-        e = launch_pdl(gateup_tok_kernel<NXC, TS>, n, kGuThreads, gsmem, st, A);
+        e = launch_pdl(gateup_tok_kernel<NXC, TS, BITS>, n, kGuThreads, gsmem, st, A);
     if (e == cudaSuccess)
-        e = launch_pdl(down_tok_kernel<TS>, n, kDnThreads, smem, st, A, H);
+        e = launch_pdl(down_tok_kernel<TS, BITS>, n, kDnThreads, smem, st, A, H);
     return e;
+}
+
+template <int BITS>
+static cudaError_t experts_bits(const Shape &s, const TokArgs &A, int n, size_t gsmem, size_t smem, cudaStream_t st)
+{
+    const bool f16 = s.qscale == MOE_F16;
+    if (s.H == 1024)
+        return f16 ? experts_go<1, __half, BITS>(A, n, gsmem, smem, s.H, st)
+                   : experts_go<1, float, BITS>(A, n, gsmem, smem, s.H, st);
+    return f16 ? experts_go<2, __half, BITS>(A, n, gsmem, smem, s.H, st)
+               : experts_go<2, float, BITS>(A, n, gsmem, smem, s.H, st);
 }
 
 cudaError_t launch_experts(const Shape &s, const Bufs &b, const ExpertSrc &src, const Routing &R, void *y,
@@ -1111,11 +1187,7 @@ cudaError_t launch_experts(const Shape &s, const Bufs &b, const ExpertSrc &src, 
     TokArgs A{b.xrec, b.xrs, src, R, b.arec, b.ars, static_cast<__nv_bfloat16 *>(y), y32,
               s.E, s.k, s.I, s.Is, log2i(s.G)};
     const size_t smem = down_smem(s, n), gsmem = gateup_smem(s, n);
-    const bool f16 = s.qscale == MOE_F16;
-    if (s.H == 1024)
-        return f16 ? experts_go<1, __half>(A, n, gsmem, smem, s.H, st)
-                   : experts_go<1, float>(A, n, gsmem, smem, s.H, st);
-    return f16 ? experts_go<2, __half>(A, n, gsmem, smem, s.H, st) : experts_go<2, float>(A, n, gsmem, smem, s.H, st);
+    return s.bits == 8 ? experts_bits<8>(s, A, n, gsmem, smem, st) : experts_bits<4>(s, A, n, gsmem, smem, st);
 }
 
 } // namespace tok

@@ -609,7 +609,7 @@ bool eligible(const Shape &s, int T)
 {
     if (kernel_path() != 0 || T < kMinTokens || T > 65536)
         return false;
-    if (s.act != MOE_BF16 || s.H % 128 || s.I % 64 || s.Is % 64 || s.Is == 0)
+    if (s.act != MOE_BF16 || s.bits != 4 || s.H % 128 || s.I % 64 || s.Is % 64 || s.Is == 0)
         return false;
     if (encode_fn() == nullptr)
         return false;

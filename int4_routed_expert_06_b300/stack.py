@@ -16,16 +16,6 @@ import torch
 from . import binding as B
 
 
-def layer_input(x: torch.Tensor, eps: float = 1e-6) -> torch.Tensor:
-    """The input of the next MoE layer in a stack: the residual stream x
-    [T, H] scaled to unit RMS per token (fp32 arithmetic, result in x's
-    dtype).  Without a norm between layers the SwiGLU experts, whose output
-    grows with the square of their input, drive a residual chain of random
-    layers to overflow within a few dozen layers."""
-    xf = x.float()
-    return (xf * torch.rsqrt(xf.pow(2).mean(dim=-1, keepdim=True) + eps)).to(x.dtype)
-
-
 class PooledStack:
     def __init__(self, shape, n_layers: int, slots_per_layer: int,
                  layer_weights: Callable[[int], Dict[str, torch.Tensor]], device: str = "cuda"):

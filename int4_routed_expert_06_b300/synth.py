@@ -56,6 +56,7 @@ class MoEShape:
     pool_slots: int = 0   # slots per layer in a bounded pool (0 = all resident)
     weight_seed: int = 0
     router_on_grid: bool = False  # router and shared gate drawn, then put on the affine 4-bit grid
+    bits: int = 4                 # code width of the expert weights (MLX affine int4 or int8)
 
 
 TINY = MoEShape("tiny", 64, 8, 2, 32, 32, 32, "f32", "f32", "f32", 0.05, 0.05,
@@ -69,7 +70,12 @@ STACK_80B = MoEShape("80b-stack", 2048, 512, 10, 512, 512, 64, "bf16", "bf16", "
 PREFILL_80B = MoEShape("80b-prefill", 2048, 512, 10, 512, 512, 64, "bf16", "bf16",
                        "f16", 0.02, 0.02, tokens=4096, zipf_s=1.1, weight_seed=2)
 
-SHAPES = {s.name: s for s in (TINY, DEC_35B, DEC_80B, STACK_80B, PREFILL_80B)}
+# The same layers with affine int8 codes (page 2 "Relation to TurboFieldfare"
+# names int4 and int8 group quantisation).
+DEC_35B_INT8 = dataclasses.replace(DEC_35B, name="35b-dec-int8", bits=8)
+DEC_80B_INT8 = dataclasses.replace(DEC_80B, name="80b-dec-int8", bits=8)
+
+SHAPES = {s.name: s for s in (TINY, DEC_35B, DEC_80B, STACK_80B, PREFILL_80B, DEC_35B_INT8, DEC_80B_INT8)}
 
 # Seeds of the per-step activations (decode: 1000 + step; stack: 5000 + step;
 # prefill: 7; tiny: 0).
@@ -108,26 +114,30 @@ def _randn(shape, std, gen, device) -> torch.Tensor:
     return torch.randn(shape, generator=gen, device=device, dtype=torch.float32) * std
 
 
-def quantise_affine4(w: torch.Tensor, group: int, scale_dtype: torch.dtype):
-    """Min-max affine 4-bit quantiser (checkpoint preparation, not the forward).
+def quantise_affine4(w: torch.Tensor, group: int, scale_dtype: torch.dtype, bits: int = 4):
+    """Min-max affine quantiser with b-bit codes, b = bits (4 or 8; checkpoint
+    preparation, not the forward).
 
-    w: [..., out, in] float32.  Per group of `group` input columns:
-    scale = (max - min) / 15, bias = min, code = clamp(round_half_even(
-    (w - bias) / scale), 0, 15) (code 0 where the group is constant).
-    Returns (packed int32 [..., out, in/8] holding uint32 bit patterns,
+    w: [..., out, in] float32.  Per group of `group` input columns, with
+    m = 2^b - 1: scale = (max - min) / m, bias = min, code = clamp(
+    round_half_even((w - bias) / scale), 0, m) (code 0 where the group is
+    constant).  Returns (packed int32 [..., out, in*b/32] holding uint32 bit
+    patterns, 32/b codes a word with the lowest column in the lowest bits,
     scale [..., out, in/G], bias [..., out, in/G]) in `scale_dtype`.
     """
     *lead, n_out, n_in = w.shape
-    assert n_in % group == 0 and n_in % 8 == 0
+    per = 32 // bits
+    levels = (1 << bits) - 1
+    assert n_in % group == 0 and n_in % per == 0
     g = w.reshape(*lead, n_out, n_in // group, group)
     lo = g.amin(dim=-1)
     hi = g.amax(dim=-1)
-    scale = (hi - lo) / 15.0
+    scale = (hi - lo) / float(levels)
     safe = torch.where(scale > 0, scale, torch.ones_like(scale))
     code = torch.round((g - lo.unsqueeze(-1)) / safe.unsqueeze(-1))
     code = torch.where(scale.unsqueeze(-1) > 0, code, torch.zeros_like(code))
-    code = code.clamp_(0, 15).to(torch.int64).reshape(*lead, n_out, n_in // 8, 8)
-    shifts = torch.arange(0, 32, 4, device=w.device, dtype=torch.int64)
+    code = code.clamp_(0, levels).to(torch.int64).reshape(*lead, n_out, n_in // per, per)
+    shifts = torch.arange(0, 32, bits, device=w.device, dtype=torch.int64)
     words = (code << shifts).sum(dim=-1)                       # 0 .. 2^32-1
     words = torch.where(words >= 2**31, words - 2**32, words)  # same bits as int32
     return words.to(torch.int32), scale.to(scale_dtype), lo.to(scale_dtype)
@@ -140,7 +150,7 @@ def _quantised_matrix_stack(n, n_out, n_in, shape: MoEShape, gen, device, chunk=
     for s0 in range(0, n, chunk):
         m = min(chunk, n - s0)
         w = _randn((m, n_out, n_in), shape.w_std, gen, device)
-        q, s, b = quantise_affine4(w, shape.group, sd)
+        q, s, b = quantise_affine4(w, shape.group, sd, shape.bits)
         qs.append(q), ss.append(s), bs.append(b)
         del w
     return torch.cat(qs), torch.cat(ss), torch.cat(bs)
@@ -212,6 +222,7 @@ def make_layer(shape: MoEShape, seed: Optional[int] = None, device="cpu") -> Dic
     """
     seed = shape.weight_seed if seed is None else seed
     layer = make_router(shape, seed, device)
+    layer["bits"] = shape.bits
     layer.update(make_experts(shape, shape.n_experts, shape.inter, seed * 31 + 1, device))
     if shape.shared_inter > 0:
         sh = make_experts(shape, 1, shape.shared_inter, seed * 31 + 2, device)
@@ -239,16 +250,16 @@ def shuffled_slots(n_experts: int, seed: int, n_slots: Optional[int] = None) -> 
     return torch.randperm(n_slots, generator=gen)[:n_experts].to(torch.int32)
 
 
-def bytes_per_qmatrix(n_out: int, n_in: int, group: int, scale_bytes: int) -> int:
-    """Stored bytes of one int4 matrix: packed codes + scale + bias."""
-    return n_out * n_in // 2 + 2 * n_out * (n_in // group) * scale_bytes
+def bytes_per_qmatrix(n_out: int, n_in: int, group: int, scale_bytes: int, bits: int = 4) -> int:
+    """Stored bytes of one quantised matrix: packed codes + scale + bias."""
+    return n_out * n_in * bits // 8 + 2 * n_out * (n_in // group) * scale_bytes
 
 
 def expert_bytes(shape: MoEShape, inter: Optional[int] = None) -> int:
     I = shape.inter if inter is None else inter
     sb = 2 if shape.qscale == "f16" else 4
-    return (2 * bytes_per_qmatrix(I, shape.hidden, shape.group, sb)
-            + bytes_per_qmatrix(shape.hidden, I, shape.group, sb))
+    return (2 * bytes_per_qmatrix(I, shape.hidden, shape.group, sb, shape.bits)
+            + bytes_per_qmatrix(shape.hidden, I, shape.group, sb, shape.bits))
 
 
 def active_expert_bytes(shape: MoEShape) -> int:
@@ -259,4 +270,5 @@ def active_expert_bytes(shape: MoEShape) -> int:
 
 assert expert_bytes(DEC_80B) == 1_769_472
 assert active_expert_bytes(DEC_80B) == 19_464_192
+assert expert_bytes(DEC_80B_INT8) == 3 * (512 * 2048 + 2 * 512 * 32 * 2)
 assert math.isclose(ZIPF_BETA, 0.44)

@@ -13,8 +13,8 @@
  *   - each layer routes each token to 10 of 512 (80B) or 8 of 256 (35B)
  *     experts (page 2 "How it works");
  *   - the router and a shared expert are resident (page 2 "How it works");
- *   - weights use MLX affine int4 group quantisation, W ~= scale*q + bias
- *     per group (page 2 "Relation to TurboFieldfare");
+ *   - weights use MLX affine int4 or int8 group quantisation,
+ *     W ~= scale*q + bias per group (page 2 "Relation to TurboFieldfare");
  *   - the layer is checked against an exact CPU reference, and streaming an
  *     expert from cache or from storage never changes the result (page 2
  *     "Correctness").
@@ -26,6 +26,22 @@
 #include <math.h>
 #include <stddef.h>
 #include <stdint.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Built twice: plain (the tests' oracle), and with OpenMP, where the loops
+ * over output rows below are shared among threads.  Each output row is still
+ * computed by one thread in the same order, so both builds give the same
+ * doubles; the OpenMP build only exists to time the oracle on all cores. */
+void oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    omp_set_num_threads(n > 0 ? n : 1);
+#else
+    (void)n;
+#endif
+}
 
 /* Router: logits[t,e] = sum_h w_router[e,h] * x[t,h] + bias[e]  (bias may be
  * NULL, meaning zero), and the shared-gate logit s[t] = sum_h w_sg[h] x[t,h]
@@ -35,6 +51,7 @@ void oracle_router(int T, int H, int E, const double *x, const double *w_router,
 {
     for (int t = 0; t < T; ++t) {
         const double *xt = x + (size_t)t * H;
+#pragma omp parallel for schedule(static)
         for (int e = 0; e < E; ++e) {
             const double *we = w_router + (size_t)e * H;
             double acc = 0.0;
@@ -80,35 +97,38 @@ void oracle_topk(int E, int k, const double *logits, int32_t *idx, double *w)
         w[r] = exp(logits[idx[r]] - lmax) / den;
 }
 
-/* One dequantised weight of an affine int4 matrix [n_out, n_in] with groups
- * of G input columns: the code of column c of row o sits in word
- * q[o, c/8] at bits 4*(c%8)..4*(c%8)+3; W[o,c] = scale[o,c/G]*code + bias[o,c/G]. */
+/* One dequantised weight of an affine matrix [n_out, n_in] with b-bit codes
+ * (b = bits, 4 or 8; p = 32/b codes a word) and groups of G input columns:
+ * the code of column c of row o sits in word q[o, c/p] at bits
+ * b*(c%p) .. b*(c%p)+b-1; W[o,c] = scale[o,c/G]*code + bias[o,c/G]. */
 static double dequant(const uint32_t *q, const double *scale, const double *bias,
-                      int n_in, int G, int o, int c)
+                      int n_in, int G, int bits, int o, int c)
 {
-    uint32_t word = q[(size_t)o * (n_in / 8) + c / 8];
-    unsigned code = (word >> (4 * (c % 8))) & 0xFu;
+    const int p = 32 / bits;
+    uint32_t word = q[(size_t)o * (n_in / p) + c / p];
+    unsigned code = (word >> (bits * (c % p))) & ((1u << bits) - 1u);
     size_t g = (size_t)o * (n_in / G) + c / G;
     return scale[g] * (double)code + bias[g];
 }
 
 /* The whole dense matrix W [n_out, n_in]. */
-void oracle_dequant(int n_out, int n_in, int G, const uint32_t *q, const double *scale,
+void oracle_dequant(int n_out, int n_in, int G, int bits, const uint32_t *q, const double *scale,
                     const double *bias, double *W)
 {
     for (int o = 0; o < n_out; ++o)
         for (int c = 0; c < n_in; ++c)
-            W[(size_t)o * n_in + c] = dequant(q, scale, bias, n_in, G, o, c);
+            W[(size_t)o * n_in + c] = dequant(q, scale, bias, n_in, G, bits, o, c);
 }
 
-/* y = W v for an affine int4 matrix. */
-void oracle_qmatvec(int n_out, int n_in, int G, const uint32_t *q, const double *scale,
+/* y = W v for an affine matrix with b-bit codes. */
+void oracle_qmatvec(int n_out, int n_in, int G, int bits, const uint32_t *q, const double *scale,
                     const double *bias, const double *v, double *y)
 {
+#pragma omp parallel for schedule(static)
     for (int o = 0; o < n_out; ++o) {
         double acc = 0.0;
         for (int c = 0; c < n_in; ++c)
-            acc += dequant(q, scale, bias, n_in, G, o, c) * v[c];
+            acc += dequant(q, scale, bias, n_in, G, bits, o, c) * v[c];
         y[o] = acc;
     }
 }
@@ -117,18 +137,18 @@ static double silu(double g) { return g / (1.0 + exp(-g)); }
 
 /* One SwiGLU expert on one token: g = Wg x, u = Wu x, a = silu(g) * u,
  * y = Wd a.  Wg, Wu: [I, H]; Wd: [H, I].  work: 3*I doubles. */
-void oracle_expert(int H, int I, int G,
+void oracle_expert(int H, int I, int G, int bits,
                    const uint32_t *qg, const double *sg, const double *bg,
                    const uint32_t *qu, const double *su, const double *bu,
                    const uint32_t *qd, const double *sd, const double *bd,
                    const double *x, double *y, double *work)
 {
     double *g = work, *u = work + I, *a = work + 2 * (size_t)I;
-    oracle_qmatvec(I, H, G, qg, sg, bg, x, g);
-    oracle_qmatvec(I, H, G, qu, su, bu, x, u);
+    oracle_qmatvec(I, H, G, bits, qg, sg, bg, x, g);
+    oracle_qmatvec(I, H, G, bits, qu, su, bu, x, u);
     for (int i = 0; i < I; ++i)
         a[i] = silu(g[i]) * u[i];
-    oracle_qmatvec(H, I, G, qd, sd, bd, a, y);
+    oracle_qmatvec(H, I, G, bits, qd, sd, bd, a, y);
 }
 
 /* Token -> expert bucketing: a stable counting sort of the T*k (token, rank)

@@ -30,42 +30,69 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "moe_oracle.c")
 _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
+_OMP_PATH = os.path.join(_OUT_DIR, "liboracle_omp.so")
 _lock = threading.Lock()
 _lib = None
+_lib_omp = None
+_threads = 1
 
 _D = ctypes.POINTER(ctypes.c_double)
 _U32 = ctypes.POINTER(ctypes.c_uint32)
 _I32 = ctypes.POINTER(ctypes.c_int32)
 
 
-def build(force: bool = False) -> str:
-    """Compile moe_oracle.c into oracle/_build/liboracle.so (gcc, -O2, no fast-math)."""
-    os.makedirs(_OUT_DIR, exist_ok=True)
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
-        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+def _compile(path: str, extra, force: bool):
+    if force or not os.path.exists(path) or os.path.getmtime(path) < os.path.getmtime(_SRC):
+        tmp = path + f".{os.getpid()}.tmp"
         subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared",
-                               "-ffp-contract=off", "-o", tmp, _SRC, "-lm"])
-        os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+                               "-ffp-contract=off", *extra, "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, path)
+    return path
+
+
+def build(force: bool = False) -> str:
+    """Compile moe_oracle.c into oracle/_build/liboracle.so (gcc, -O2, no
+    fast-math), and the same source with OpenMP into liboracle_omp.so."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    _compile(_OMP_PATH, ["-fopenmp"], force)
+    return _compile(_LIB_PATH, [], force)
+
+
+def set_threads(n: int) -> None:
+    """Run the oracle's loops over output rows on n threads (n > 1 loads the
+    OpenMP build; every output is computed as in the plain build)."""
+    global _threads
+    _threads = max(1, int(n))
+    if _threads > 1:
+        lib().oracle_set_threads(_threads)
 
 
 def lib():
-    global _lib
+    global _lib, _lib_omp
     with _lock:
+        if _threads > 1:
+            if _lib_omp is None:
+                build()
+                _lib_omp = _bind(ctypes.CDLL(_OMP_PATH))
+            return _lib_omp
         if _lib is None:
-            L = ctypes.CDLL(build())
-            c_int = ctypes.c_int
-            L.oracle_router.argtypes = [c_int, c_int, c_int, _D, _D, _D, _D, _D, _D]
-            L.oracle_topk.argtypes = [c_int, c_int, _D, _I32, _D]
-            L.oracle_dequant.argtypes = [c_int, c_int, c_int, _U32, _D, _D, _D]
-            L.oracle_qmatvec.argtypes = [c_int, c_int, c_int, _U32, _D, _D, _D, _D]
-            L.oracle_expert.argtypes = [c_int, c_int, c_int] + [_U32, _D, _D] * 3 + [_D, _D, _D]
-            L.oracle_bucket.argtypes = [c_int, c_int, c_int, _I32, _I32, _I32, _I32, _I32]
-            for f in ("oracle_router", "oracle_topk", "oracle_dequant", "oracle_qmatvec",
-                      "oracle_expert", "oracle_bucket"):
-                getattr(L, f).restype = None
-            _lib = L
+            _lib = _bind(ctypes.CDLL(build()))
     return _lib
+
+
+def _bind(L):
+    c_int = ctypes.c_int
+    L.oracle_router.argtypes = [c_int, c_int, c_int, _D, _D, _D, _D, _D, _D]
+    L.oracle_topk.argtypes = [c_int, c_int, _D, _I32, _D]
+    L.oracle_dequant.argtypes = [c_int, c_int, c_int, c_int, _U32, _D, _D, _D]
+    L.oracle_qmatvec.argtypes = [c_int, c_int, c_int, c_int, _U32, _D, _D, _D, _D]
+    L.oracle_expert.argtypes = [c_int, c_int, c_int, c_int] + [_U32, _D, _D] * 3 + [_D, _D, _D]
+    L.oracle_bucket.argtypes = [c_int, c_int, c_int, _I32, _I32, _I32, _I32, _I32]
+    L.oracle_set_threads.argtypes = [c_int]
+    for f in ("oracle_router", "oracle_topk", "oracle_dequant", "oracle_qmatvec",
+              "oracle_expert", "oracle_bucket", "oracle_set_threads"):
+        getattr(L, f).restype = None
+    return L
 
 
 # ---------------------------------------------------------------- marshalling
@@ -130,19 +157,19 @@ def topk(logits, k):
     return (idx[0], w[0]) if one else (idx, w)
 
 
-def dequant(q, scale, bias, group):
+def dequant(q, scale, bias, group, bits=4):
     q, s, b = u32(q), f64(scale), f64(bias)
-    n_out, n_in = q.shape[0], q.shape[1] * 8
+    n_out, n_in = q.shape[0], q.shape[1] * (32 // bits)
     W = np.zeros((n_out, n_in))
-    lib().oracle_dequant(n_out, n_in, group, _p(q, _U32), _p(s, _D), _p(b, _D), _p(W, _D))
+    lib().oracle_dequant(n_out, n_in, group, bits, _p(q, _U32), _p(s, _D), _p(b, _D), _p(W, _D))
     return W
 
 
-def qmatvec(q, scale, bias, group, v):
+def qmatvec(q, scale, bias, group, v, bits=4):
     q, s, b, v = u32(q), f64(scale), f64(bias), f64(v)
-    n_out, n_in = q.shape[0], q.shape[1] * 8
+    n_out, n_in = q.shape[0], q.shape[1] * (32 // bits)
     y = np.zeros(n_out)
-    lib().oracle_qmatvec(n_out, n_in, group, _p(q, _U32), _p(s, _D), _p(b, _D), _p(v, _D), _p(y, _D))
+    lib().oracle_qmatvec(n_out, n_in, group, bits, _p(q, _U32), _p(s, _D), _p(b, _D), _p(v, _D), _p(y, _D))
     return y
 
 
@@ -150,12 +177,13 @@ class ExpertView:
     """One expert's nine arrays, converted once to the oracle's types."""
 
     def __init__(self, mats: dict, e: int, prefix: str = ""):
+        self.bits = int(mats.get("bits", 4))
         self.m = []
         for name in ("gate", "up", "down"):
             self.m += [u32(mats[prefix + "q_" + name][e]), f64(mats[prefix + "s_" + name][e]),
                        f64(mats[prefix + "b_" + name][e])]
         self.inter = self.m[0].shape[0]
-        self.hidden = self.m[0].shape[1] * 8
+        self.hidden = self.m[0].shape[1] * (32 // self.bits)
 
 
 def expert(view: ExpertView, group: int, x):
@@ -167,7 +195,7 @@ def expert(view: ExpertView, group: int, x):
     args = []
     for j, a in enumerate(view.m):
         args.append(_p(a, _U32 if j % 3 == 0 else _D))
-    lib().oracle_expert(H, I, group, *args, _p(x, _D), _p(y, _D), _p(work, _D))
+    lib().oracle_expert(H, I, group, view.bits, *args, _p(x, _D), _p(y, _D), _p(work, _D))
     return y
 
 

@@ -6,7 +6,7 @@ import torch
 
 import bench
 from int4_routed_expert_06_b300 import synth
-from int4_routed_expert_06_b300.stack import layer_input
+from bench import layer_input
 
 
 def test_metric_names_follow_the_workload():

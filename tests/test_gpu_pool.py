@@ -16,7 +16,8 @@ import torch
 from gpu_util import assert_close, near_tie_tokens
 from int4_routed_expert_06_b300 import binding as B
 from int4_routed_expert_06_b300 import synth
-from int4_routed_expert_06_b300.stack import PooledStack, layer_input
+from bench import layer_input
+from int4_routed_expert_06_b300.stack import PooledStack
 from oracle import oracle as O
 from oracle.slot_policy import SlotPolicy
 

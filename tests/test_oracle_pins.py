@@ -6,6 +6,7 @@ sort) or a hand-computed trace, chosen so that a plausible slip (a dropped
 term, a wrong sign, a swapped nibble order, a transposed operand, a reversed
 tie-break) fails at least one of them.
 """
+import dataclasses
 import itertools
 import json
 import os
@@ -126,6 +127,71 @@ def test_expert_matches_dense_numpy():
         np.testing.assert_allclose(O.expert(view, shp.group, x), ref, rtol=1e-12, atol=1e-14)
 
 
+def test_dequant_int8_closed_forms_and_byte_placement():
+    """8-bit codes: four a word, the lowest column in the lowest byte."""
+    n_out, n_in, G = 4, 64, 32
+    rng = np.random.default_rng(3)
+    s = rng.uniform(0.001, 0.01, size=(n_out, n_in // G))
+    b = rng.normal(size=(n_out, n_in // G))
+    zero = np.zeros((n_out, n_in // 4), np.uint32)
+    np.testing.assert_array_equal(O.dequant(zero, s, b, G, bits=8), np.repeat(b, G, axis=1))
+    full = np.full((n_out, n_in // 4), 0xFFFFFFFF, np.uint32)
+    np.testing.assert_allclose(O.dequant(full, s, b, G, bits=8), np.repeat(255 * s + b, G, axis=1), rtol=1e-15)
+    # one code in one known place: row 1, column 45 -> word 11, byte 1; group 1
+    one = zero.copy()
+    one[1, 11] = 0xC8 << 8
+    D = O.dequant(one, s, b, G, bits=8)
+    expect = np.repeat(b, G, axis=1)
+    expect[1, 45] += 200 * s[1, 1]
+    np.testing.assert_allclose(D, expect, rtol=1e-15)
+    # the same word read as 4-bit codes is a different matrix
+    assert not np.allclose(O.dequant(one, s, b, G, bits=4)[:, :64], D)
+
+
+@pytest.mark.parametrize("sd,group", [("f32", 64), ("f16", 64), ("f32", 32)])
+def test_dequant_int8_round_trip_within_half_step(sd, group):
+    g = torch.Generator().manual_seed(12)
+    w = torch.randn((16, 256), generator=g) * 0.05
+    q, s, b = synth.quantise_affine4(w, group, synth.torch_dtype(sd), bits=8)
+    assert q.shape == (16, 64)
+    W = O.dequant(q, s, b, group, bits=8)
+    step = np.repeat(O.f64(s), group, axis=1)
+    err = np.abs(W - w.double().numpy())
+    slack = 0.0 if sd == "f32" else 2.0 ** -10 * (np.abs(np.repeat(O.f64(b), group, 1)) + 255 * step)
+    assert np.all(err <= step * (0.5 + 1e-5) + slack + 1e-12)
+    # 255 levels: the step is about 1/17 of the 4-bit step of the same rows
+    _, s4, _ = synth.quantise_affine4(w, group, synth.torch_dtype(sd), bits=4)
+    np.testing.assert_allclose(O.f64(s4) / O.f64(s), 17.0, rtol=2e-3)
+
+
+def test_qmatvec_int8_matches_numpy_matmul():
+    rng = np.random.default_rng(4)
+    n_out, n_in, G = 10, 256, 64
+    q = rng.integers(0, 2**32, size=(n_out, n_in // 4), dtype=np.uint32)
+    s = rng.uniform(0.0001, 0.002, size=(n_out, n_in // G))
+    b = rng.normal(scale=0.02, size=(n_out, n_in // G))
+    v = rng.normal(size=n_in)
+    codes = np.stack([(q >> (8 * j)) & 0xFF for j in range(4)], axis=2).reshape(n_out, n_in)
+    W = codes * np.repeat(s, G, axis=1) + np.repeat(b, G, axis=1)   # built here, not by the oracle
+    np.testing.assert_allclose(O.qmatvec(q, s, b, G, v, bits=8), W @ v, rtol=1e-12, atol=1e-14)
+
+
+def test_expert_int8_matches_dense_numpy():
+    shp = dataclasses.replace(synth.TINY, bits=8)
+    ex = synth.make_experts(shp, 2, shp.inter, seed=6)
+    ex["bits"] = 8
+    assert ex["q_gate"].shape[-1] == shp.hidden // 4
+    x = np.random.default_rng(5).normal(size=shp.hidden)
+    for e in range(2):
+        view = O.ExpertView(ex, e)
+        assert view.bits == 8 and view.hidden == shp.hidden
+        Wg, Wu, Wd = (O.dequant(ex["q_" + m][e], ex["s_" + m][e], ex["b_" + m][e], shp.group, bits=8)
+                      for m in ("gate", "up", "down"))
+        g, u = Wg @ x, Wu @ x
+        ref = Wd @ (g * sps.expit(g) * u)
+        np.testing.assert_allclose(O.expert(view, shp.group, x), ref, rtol=1e-12, atol=1e-14)
+
+
 # --------------------------------------------------------------- layer
 
 def _tiny_layer():
@@ -242,3 +308,19 @@ def test_slot_policy_exhaustion_and_layers_independent():
     pol.lookup(0, [0, 1])
     pol.lookup(1, [2, 3])
     assert pol.table[0][:4] == [0, 1, -1, -1] and pol.table[1][:4] == [-1, -1, 0, 1]
+
+
+def test_openmp_build_gives_the_same_doubles():
+    """The all-cores build of the oracle (OpenMP over output rows, used only
+    to time the CPU baseline) computes every output exactly as the plain build."""
+    for shp, x in ((synth.TINY, synth.make_x(synth.TINY, synth.TINY_X_SEED)),
+                   (synth.DEC_35B, synth.make_x(synth.DEC_35B, 1234, 1))):
+        w = synth.make_layer(shp)
+        ref = O.Layer(w, shp.group, shp.top_k).forward(x)
+        O.set_threads(4)
+        try:
+            got = O.Layer(w, shp.group, shp.top_k).forward(x)
+        finally:
+            O.set_threads(1)
+        assert np.array_equal(got["y"], ref["y"]) and np.array_equal(got["idx"], ref["idx"])
+        assert np.array_equal(got["logits"], ref["logits"])
