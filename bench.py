@@ -26,7 +26,11 @@ at batch 1); no collective touches the data path.
 `--workload 35b-dec`, `80b-dec-int8` and `35b-dec-int8` time the same decode
 loop on the 35B-shaped layer and on both layers with affine int8 codes.
 
-Two more workloads print their own line (not the default):
+Three more workloads print their own line (not the default):
+
+- `--workload 80b-batch`: tokens/s of one 80B-shaped layer call of T = 1 ..
+  64 tokens on each kernel path (generic kernels, tcgen05 grouped GEMMs, and
+  the default choice).
 
 - `--workload 80b-prefill`: one step = one 4096-token layer call (Zipf-skewed
   routing, tcgen05 grouped GEMMs); tokens/s and TFLOP/s on algorithmic flops
@@ -553,6 +557,83 @@ def routing_trace(shape, layer: int, tokens: int):
     return torch.topk(logits, shape.top_k, dim=1).indices.to(torch.int32)
 
 
+def run_batch_sweep(args, shape):
+    """Small decode batches: tokens/s of one 80B-shaped layer call at T = 1 ...
+    64 on each kernel path (1: generic kernels, 2: tcgen05 grouped GEMMs from
+    T = 2, 0: the default choice).  Each point is a CUDA graph of calls whose
+    seeded x rotate through layer copies larger than L2 together."""
+    from int4_routed_expert_06_b300 import binding as B
+    from int4_routed_expert_06_b300 import build as _build
+    _build.build()
+    torch.cuda.set_device(0)
+    w = synth.make_layer(shape, device="cuda")
+    slots = synth.shuffled_slots(shape.n_experts, shape.weight_seed)
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    layer_bytes = shape.n_experts * synth.expert_bytes(shape)
+    R = args.replicas if args.replicas > 0 else max(2, math.ceil(3 * l2 / layer_bytes) + 1)
+    dl = B.DeviceLayer(shape, w, slots, replicas=R)
+    cfg = dl.cfg
+    Ts = [1, 2, 4, 8, 16, 32, 64]
+    calls = 8 * R
+    stream = torch.cuda.Stream()
+    table = []
+    with ClockSampler(0) as clk:
+        for T in Ts:
+            xs = synth.make_x(shape, 4000 + T, T * calls, device="cuda")
+            ys = torch.empty((T * calls, shape.hidden), dtype=torch.bfloat16, device="cuda")
+            row = {"T": T}
+            for path in (1, 2, 0):
+                if T == 1 and path == 2:
+                    continue
+                B.moe_set_kernel_path(path)
+                try:
+                    nb = B.moe_layer_workspace_bytes(cfg, T)
+                    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+
+                    def run():
+                        for j in range(calls):
+                            B.moe_layer_forward(cfg, dl.struct(j % R), xs[j * T:(j + 1) * T], T,
+                                                ys[j * T:(j + 1) * T], None, None, None, ws, nb)
+
+                    with torch.cuda.stream(stream):
+                        run()
+                    torch.cuda.synchronize()
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, stream=stream):
+                        run()
+                finally:
+                    B.moe_set_kernel_path(0)
+                with torch.cuda.stream(stream):
+                    for _ in range(max(3, args.warmup)):
+                        g.replay()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    for _ in range(args.steps):
+                        g.replay()
+                    e1.record(stream)
+                torch.cuda.synchronize()
+                us = e0.elapsed_time(e1) * 1e3 / (args.steps * calls)
+                row[{1: "generic", 2: "grouped_gemm", 0: "default"}[path]] = {
+                    "us_per_call": round(us, 2), "tokens_per_s": round(T / (us * 1e-6), 1)}
+                del g
+            table.append(row)
+    if B.moe_get_device_error(stream) != 0:
+        raise RuntimeError("a kernel recorded a device error during the sweep")
+    best = max(r["default"]["tokens_per_s"] for r in table)
+    line = {
+        "metric": "routed-MoE layer tokens/s at small decode batches (80B layer, one call of T tokens)",
+        "value": table[-1]["default"]["tokens_per_s"], "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": max(3, args.warmup), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 tensor-core GEMMs (grouped) / s32 dp4a and f32 (single-token, generic)", "data": "synthetic",
+        "config": {"workload": workload_desc(shape).replace("batch-1 decode", "decode batches T = 1..64"),
+                   "value_at": "T = 64, default path", "calls_per_graph": calls,
+                   "l2": f"calls rotate through {R} layer copies ({R * layer_bytes / 1e9:.1f} GB)"},
+        "sweep": table, "best_default_tokens_per_s": best,
+        "clocks": clk.summary(), "gpu_launches": None,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_policy_study(args):
     """Hit rate of the slot pool's host policy (the library's own
     slot_pool_lookup) against pool fraction, Zipf skew and eviction rule, on
@@ -615,7 +696,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="80b-dec",
                     choices=["80b-dec", "35b-dec", "80b-dec-int8", "35b-dec-int8", "80b-prefill", "80b-stack",
-                             "policy-study"])
+                             "80b-batch", "policy-study"])
     ap.add_argument("--tokens", type=int, default=1000, help="decode tokens per bench step")
     ap.add_argument("--replicas", type=int, default=0, help="layer copies to rotate through (0 = >= 3x L2)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -629,6 +710,10 @@ def main():
     if args.workload == "policy-study":
         if rank == 0:  # host-only: the pool's eviction rules on routing traces
             run_policy_study(args)
+        return
+    if args.workload == "80b-batch":
+        if rank == 0:
+            run_batch_sweep(args, synth.DEC_80B)
         return
     shape = synth.SHAPES[args.workload]
 

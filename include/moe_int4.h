@@ -323,9 +323,12 @@ const char *moe_version(void);
 /* Kernel selection for calls made from the calling host thread (the setting
  * is per thread): 0 (default) uses the single-token kernels for T = 1 and
  * the tcgen05 grouped GEMMs for T >= 64 where the shape allows; 1 forces the
- * generic kernels everywhere.  The two compute the same function (the
- * pages' practice of checking fast against scalar kernels); tests compare
- * both against the CPU oracle.  MOE_ERR_INVALID_ARG for other values. */
+ * generic kernels everywhere; 2 is 0 with the grouped GEMMs from T = 2 up
+ * (small decode batches on the tensor cores).  All compute the same
+ * function (the pages' practice of checking fast against scalar kernels);
+ * tests compare each against the CPU oracle.  The workspace size a call
+ * needs depends on the path: query moe_*_workspace_bytes under the same
+ * setting.  MOE_ERR_INVALID_ARG for other values. */
 moe_status moe_set_kernel_path(int32_t path);
 
 /* Test hooks, process-wide, for exercising the failure path of bounded

@@ -99,7 +99,7 @@ static Ws layer_ws(const Shape &s, int T)
     w.tok = o;    o += T == 1 ? align256(tok::bufs_bytes(s)) : 0;
     w.hist = o;   o += align256(sizeof(int32_t) * (size_t)bucket_chunks(T * s.k) * s.E);
     w.pre = o;
-    if (T >= prefill::kMinTokens && s.bits == 4 && s.H % 128 == 0 && s.I % 64 == 0 && s.Is % 64 == 0 && s.Is > 0)
+    if (prefill::wanted(s, T))
         o += align256(prefill::layout(s, T).total);
     w.total = o;
     return w;
@@ -124,8 +124,8 @@ const char *moe_version(void) { return "moe_int4 0.2 (sm_103a)"; }
 
 moe_status moe_set_kernel_path(int32_t path)
 {
-    if (path != 0 && path != 1)
-        return fail(MOE_ERR_INVALID_ARG, "moe_set_kernel_path: path %d must be 0 or 1", path);
+    if (path < 0 || path > 2)
+        return fail(MOE_ERR_INVALID_ARG, "moe_set_kernel_path: path %d must be 0, 1 or 2", path);
     g_kernel_path = path;
     return MOE_OK;
 }

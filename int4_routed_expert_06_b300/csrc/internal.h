@@ -96,16 +96,21 @@ cudaError_t launch_experts(const Shape &s, const Bufs &b, const ExpertSrc &src, 
 } // namespace tok
 
 namespace prefill {
-// Calls with at least this many tokens take the grouped-GEMM path.
+// Calls with at least this many tokens take the grouped-GEMM path (kernel
+// path 0); kernel path 2 takes it from 2 tokens up.
 constexpr int kMinTokens = 64;
+int min_tokens();
 // Byte offsets of the prefill buffers inside a workspace region.
 struct Layout {
     size_t counts, offsets, perm_tok, perm_rank, hist, inv, wpair, units_gu, units_dn, n_units, xs, act, pout,
         total;
 };
 Layout layout(const Shape &s, int T);
-// bf16 activations, H a multiple of 128, I and I_s multiples of 64, a shared
-// expert, a Blackwell (sm_10x) device, T >= kMinTokens.
+// The shape and token count take the grouped GEMMs under the calling
+// thread's kernel path: bf16 activations, 4-bit codes, H a multiple of 128,
+// I and I_s multiples of 64, a shared expert, T >= min_tokens().
+bool wanted(const Shape &s, int T);
+// wanted() on a Blackwell (sm_10x) device with the tensor-map encoder.
 bool eligible(const Shape &s, int T);
 cudaError_t experts_forward(const Shape &s, const ExpertSrc &src, const void *x, int T, const int32_t *idx,
                             const float *topk_w, const float *sg, void *y, float *y32, char *ws, cudaStream_t st);

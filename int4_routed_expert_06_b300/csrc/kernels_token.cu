@@ -236,9 +236,11 @@ __device__ __forceinline__ void store_chunk4(const float v[4], unsigned char *re
     }
 }
 
-// sum_c q_c * (256 xh_c + xl_c) over one chunk of 32 codes (exact integer),
-// in four short dp4a chains.
-__device__ __forceinline__ int chunk_idot(uint4 q, const Chunk &c)
+// 16 sum_c q_c * (256 xh_c + xl_c) over one chunk of 32 codes (exact
+// integer, |value| < 2^28), in four short dp4a chains.  The odd nibbles stay
+// in place (16 q, one LOP3 a word instead of a shift and a LOP3): their
+// chains carry 16x, so the even chains are scaled by 16 to match.
+__device__ __forceinline__ int chunk_idot16(uint4 q, const Chunk &c)
 {
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
     const uint32_t he[4] = {c.he.x, c.he.y, c.he.z, c.he.w};
@@ -249,19 +251,20 @@ __device__ __forceinline__ int chunk_idot(uint4 q, const Chunk &c)
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
         const uint32_t ev = w[m] & 0x0F0F0F0Fu;
-        const uint32_t od = (w[m] >> 4) & 0x0F0F0F0Fu;
+        const uint32_t od = w[m] & 0xF0F0F0F0u;
         h0 = dp4a_us(ev, he[m], h0);
         h1 = dp4a_us(od, ho[m], h1);
         l0 = dp4a_uu(ev, le[m], l0);
         l1 = dp4a_uu(od, lo[m], l1);
     }
-    return (h0 + h1) * 256 + (l0 + l1);
+    return (h0 * 16 + h1) * 256 + (l0 * 16 + l1);
 }
 
-// s * sum_c q_c v_c + b * sum_c v_c for one chunk.
+// s * sum_c q_c v_c + b * sum_c v_c for one chunk.  (16 D) sx / 16 rounds
+// exactly as D sx: scaling by a power of two commutes with rounding.
 __device__ __forceinline__ float chunk_term(uint4 q, const Chunk &c, float s, float b)
 {
-    const float D = (float)chunk_idot(q, c) * c.sx;
+    const float D = (float)chunk_idot16(q, c) * c.sx * 0.0625f;
     return fmaf(s, D, b * c.X);
 }
 
@@ -301,8 +304,9 @@ template <int BITS>
 __device__ __forceinline__ float row_chunk_term(const unsigned char *row, int ch, const Chunk &c, float s, float b)
 {
     const uint4 *q = reinterpret_cast<const uint4 *>(row);
-    const int D = BITS == 8 ? chunk_idot8(q[2 * ch], q[2 * ch + 1], c) : chunk_idot(q[ch], c);
-    return fmaf(s, (float)D * c.sx, b * c.X);
+    const float D = BITS == 8 ? (float)chunk_idot8(q[2 * ch], q[2 * ch + 1], c) * c.sx
+                              : (float)chunk_idot16(q[ch], c) * c.sx * 0.0625f;
+    return fmaf(s, D, b * c.X);
 }
 
 // ------------------------------------------------------------ top-k
@@ -1062,7 +1066,7 @@ constexpr size_t kSmemLimitAlone = 200 * 1024;
 
 bool eligible(const Shape &s)
 {
-    if (kernel_path() != 0)
+    if (kernel_path() == 1)
         return false;
     if (s.act != MOE_BF16 || s.router != MOE_BF16 || (s.bits != 4 && s.bits != 8))
         return false;

@@ -28,12 +28,19 @@ namespace prefill {
 
 constexpr int kNch = 256;        // tokens per unit (MMA N <= 256)
 constexpr int kBK = 64;          // K per pipeline stage (one 128-byte swizzle atom of bf16)
-constexpr int kStages = 4;
+constexpr int kStages = 3;       // A (dequantised) and B (token) tiles
+constexpr int kCStages = 3;      // staged code tiles (run ahead of the dequant)
+constexpr int kCK = 256;         // K of one code stage: 128-byte row pieces (whole lines)
 constexpr int kBoxRows = 32;     // TMA box: 32 rows x 64 bf16
-constexpr int kThreads = 320;    // warps 0-3 dequant, 4 TMA, 5 MMA, 6-9 epilogue
+// warps 0-15 dequant, 16 weight TMA, 17 token TMA, 18 MMA, 19-22 epilogue
+constexpr int kDqWarps = 16, kCodeWarp = 16, kRowWarp = 17, kMmaWarp = 18;
+constexpr int kThreads = 32 * 23;
 constexpr uint32_t kATile = 128 * 128;         // 16 KB
 constexpr uint32_t kBTile = kNch * 128;        // 32 KB
-constexpr uint32_t kSmem = kStages * (kATile + kBTile) + 1024;
+constexpr uint32_t kCTile = 128 * (kCK / 2);   // 16 KB: 128 rows x 256 codes
+constexpr uint32_t kSTile = 16 * 1024;         // a unit's scale and bias rows (at most 4 x 64 rows x 64 B)
+constexpr uint32_t kPTile = 16 * 1024;         // the same as (scale, bias) pairs [group][128 rows] (<= 32 groups)
+constexpr uint32_t kSmem = kStages * (kATile + kBTile) + kCStages * kCTile + kSTile + kPTile + 1024;
 constexpr uint64_t kWaitNs = 500ull * 1000 * 1000; // 0.5 s bound on any single wait
 
 struct Unit {
@@ -41,6 +48,7 @@ struct Unit {
     int ft;   // feature tile: gate/up 64 features (128 interleaved rows), down 128 output rows
     int j0;   // first row of the unit in the B source (sorted pair index, or token for the shared expert)
     int n;    // tokens (1..256)
+    int slot; // pool slot of the expert (0 for the shared expert), -1 when not resident
 };
 
 // ------------------------------------------------------------ PTX helpers
@@ -187,7 +195,8 @@ __global__ void pair_prep_kernel(const int32_t *__restrict__ perm_tok, const int
 // their units in that order after the shared expert's.  Unit order within an
 // expert: token chunk major, feature tile minor.  E <= 1024.
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ counts,
-                                                    const int32_t *__restrict__ offsets, int E, int T,
+                                                    const int32_t *__restrict__ offsets,
+                                                    const int32_t *__restrict__ table, int n_slots, int E, int T,
                                                     int n_ft, int n_ft_sh, int has_shared, Unit *__restrict__ units,
                                                     int32_t *__restrict__ n_units)
 {
@@ -226,14 +235,15 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
         int u = 0;
         for (int c0 = 0; c0 < T; c0 += kNch)
             for (int ft = 0; ft < n_ft_sh; ++ft)
-                units[u++] = {-1, ft, c0, min(kNch, T - c0)};
+                units[u++] = {-1, ft, c0, min(kNch, T - c0), 0};
     }
     if (e < E && nu > 0) {
         int u = sh_units + s_scan[e] - nu;
         const int base = offsets[ex], cnt = s_cnt[ex];
+        const int sl = table[ex], slot = sl >= 0 && sl < n_slots ? sl : -1;
         for (int c0 = 0; c0 < cnt; c0 += kNch)
             for (int ft = 0; ft < n_ft; ++ft)
-                units[u++] = {ex, ft, base + c0, min(kNch, cnt - c0)};
+                units[u++] = {ex, ft, base + c0, min(kNch, cnt - c0), slot};
     }
     if (e == 1023)
         *n_units = sh_units + s_scan[1023];
@@ -271,73 +281,105 @@ struct GemmArgs {
     float *pout;         // down output [T*k + T, H]
 };
 
-// 128 weight rows x 64 K of one stage, dequantised to bf16 into the swizzled
-// K-major tile (row r at r*128 bytes, 16-byte chunk c at position c ^ (r&7)).
-template <typename TS>
-__device__ __forceinline__ void dequant_row(const uint32_t *__restrict__ q, const TS *__restrict__ sc,
-                                            const TS *__restrict__ bi, int k0, int G, unsigned char *tile, int r)
+// Tensor maps of the weight side of one GEMM kind, over the fixed-stride
+// pool (3-D: bytes or scale groups of a row, rows, slot) and over the shared
+// blob (slot extent 1).  Gate/up: codes of W_g, W_u (boxes of 64 rows x 128
+// bytes = 256 K: whole 128-byte lines), and the scale and bias rows of W_g,
+// W_u (64 rows x all groups).  Down: codes of W_d (128 rows x 128 bytes), its
+// scale and bias rows (128 rows x all groups).
+struct WMaps {
+    CUtensorMap routed[6]; // gate/up: qg qu sg bg su bu; down: qd sd bd
+    CUtensorMap shared[6];
+};
+
+// One stage of one tile row quarter: 16 codes (two code words, columns
+// k0 + 16q .. + 15, one quantisation group) -> 16 bf16 w = s q + b (fp32
+// arithmetic, one rounding), written as 16-byte chunks 2q, 2q + 1 of row r
+// of the swizzled K-major tile (chunk c at position c ^ (r & 7)).
+__device__ __forceinline__ void dequant_quarter(uint2 qw, float s, float b, unsigned char *row, int r, int q)
 {
-    const uint4 w0 = __ldg(reinterpret_cast<const uint4 *>(q + k0 / 8));
-    const uint4 w1 = __ldg(reinterpret_cast<const uint4 *>(q + k0 / 8) + 1);
-    const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-    unsigned char *row = tile + r * 128;
+    const uint32_t w[2] = {qw.x, qw.y};
+    const float s16 = 16.f * s, b16 = b - s16;
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const int g = (k0 + 32 * half) / G;
-        const float s = to_f32(sc[g]), b = to_f32(bi[g]);
-        const float s16 = 16.f * s, b16 = b - s16;
+    for (int cc = 0; cc < 2; ++cc) { // 16-byte chunk = 8 columns = one code word
+        const uint32_t word = w[cc];
+        const uint32_t lo = ((word << 3) & 0x78787878u) | 0x80808080u;
+        const uint32_t hi = ((word >> 1) & 0x78787878u) | 0x80808080u;
+        uint32_t packed[4];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) { // 16-byte chunk = 8 columns = one code word
-            const uint32_t word = w[half * 4 + cc];
-            const uint32_t lo = ((word << 3) & 0x78787878u) | 0x80808080u;
-            const uint32_t hi = ((word >> 1) & 0x78787878u) | 0x80808080u;
-            uint32_t packed[4];
-#pragma unroll
-            for (int bb = 0; bb < 4; ++bb) {
-                const uint32_t sel = 0x7044u | (uint32_t)(bb << 8);
-                const float f0 = __uint_as_float(__byte_perm(lo, 0x3F000000u, sel)); // 1 + q/16, column 2bb
-                const float f1 = __uint_as_float(__byte_perm(hi, 0x3F000000u, sel)); // column 2bb + 1
-                const float2 wv = __ffma2_rn(make_float2(f0, f1), make_float2(s16, s16), make_float2(b16, b16));
-                __nv_bfloat162 h2 = __floats2bfloat162_rn(wv.x, wv.y);
-                packed[bb] = *reinterpret_cast<uint32_t *>(&h2);
-            }
-            const int c = half * 4 + cc;
-            *reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4)) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        for (int bb = 0; bb < 4; ++bb) {
+            const uint32_t sel = 0x7044u | (uint32_t)(bb << 8);
+            const float f0 = __uint_as_float(__byte_perm(lo, 0x3F000000u, sel)); // 1 + q/16, column 2bb
+            const float f1 = __uint_as_float(__byte_perm(hi, 0x3F000000u, sel)); // column 2bb + 1
+            const float2 wv = __ffma2_rn(make_float2(f0, f1), make_float2(s16, s16), make_float2(b16, b16));
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(wv.x, wv.y);
+            packed[bb] = *reinterpret_cast<uint32_t *>(&h2);
         }
+        const int c = 2 * q + cc;
+        *reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4)) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
     }
 }
+
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void dq_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kDqWarps * 32) : "memory"); }
+
+// A unit's scale and bias of one weight row and group.
+template <typename TS> struct SBPair {
+    TS s, b;
+};
 
 template <typename TS>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_constant__ CUtensorMap tm_shared,
-                        GemmArgs A)
+                        const __grid_constant__ WMaps wm, GemmArgs A)
 {
     extern __shared__ unsigned char smem_raw[];
-    __shared__ uint64_t a_full[kStages], b_full[kStages], empty[kStages], acc_full[2], acc_empty[2];
+    __shared__ uint64_t a_full[kStages], b_full[kStages], ab_empty[kStages];
+    __shared__ uint64_t c_full[kCStages], c_empty[kCStages], s_full, s_empty;
+    __shared__ uint64_t acc_full[2], acc_empty[2];
     __shared__ uint32_t tmem_base;
     __shared__ volatile int s_abort;
+    __shared__ volatile int s_dq_fail; // set only: a dequant wait gave up (read only after dq_sync)
 
     unsigned char *smem = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     unsigned char *a_tiles = smem;
-    unsigned char *b_tiles = smem + kStages * kATile;
+    unsigned char *b_tiles = a_tiles + kStages * kATile;
+    unsigned char *c_ring = b_tiles + kStages * kBTile;
+    unsigned char *s_raw = c_ring + kCStages * kCTile;
+    SBPair<TS> *s_pair = reinterpret_cast<SBPair<TS> *>(s_raw + kSTile); // [group][128 rows]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nu = *A.n_units;
-    const int G = A.G;
+    const int G = A.G, grid = gridDim.x;
+    const uint32_t sb = sizeof(TS);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            bar_init(&a_full[s], 128);
+            bar_init(&a_full[s], kDqWarps);
             bar_init(&b_full[s], 1);
-            bar_init(&empty[s], 1);
+            bar_init(&ab_empty[s], 1);
         }
+        for (int s = 0; s < kCStages; ++s) {
+            bar_init(&c_full[s], 1);
+            bar_init(&c_empty[s], kDqWarps);
+        }
+        bar_init(&s_full, 1);
+        bar_init(&s_empty, 1);
         for (int b = 0; b < 2; ++b) {
             bar_init(&acc_full[b], 1);
             bar_init(&acc_empty[b], 128);
         }
         s_abort = 0;
+        s_dq_fail = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 5) { // TMEM: 2 accumulators x 256 fp32 columns
+    if (warp == kMmaWarp) { // TMEM: 2 accumulators x 256 fp32 columns
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&tmem_base))
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -348,77 +390,176 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = tmem_base;
 
     auto kdim = [&](const Unit &u) { return A.mode == 0 ? A.H : (u.e < 0 ? A.Is : A.I); };
+    // the unit descriptor after ui (this CTA's next), loaded a unit ahead
+    auto next_unit = [&](int ui, const Unit &cur) { return ui + grid < nu ? A.units[ui + grid] : cur; };
 
-    if (warp < 4) {
-        // ---------------- dequant producers: thread r owns tile row r
-        const int r = threadIdx.x;
-        int stage = 0;
-        uint32_t ph = 0;
-        for (int ui = blockIdx.x; ui < nu && !s_abort; ui += gridDim.x) {
-            const Unit u = A.units[ui];
-            const char *base;
-            const size_t *off;
-            if (u.e < 0) {
-                base = A.src.shared;
-                off = A.src.off_sh;
-            } else {
-                const int slot = A.src.table[u.e];
-                base = (slot >= 0 && slot < A.src.n_slots) ? A.src.pool + (size_t)slot * A.src.stride : nullptr;
-                off = A.src.off;
-                if (!base && r == 0)
-                    record_error(MOE_ERR_NOT_RESIDENT);
+    if (warp < kDqWarps) {
+        // ---------------- dequant: thread t takes tile row t / 4, K quarter t % 4.
+        // The named barrier dq_sync joins exactly these warps, so they leave the
+        // unit loop together: a failed wait sets s_dq_fail, and the decision
+        // to stop is read after the next dq_sync.
+        const int t = threadIdx.x, r = t >> 2, q = t & 3;
+        int cs = 0, as = 0;
+        uint32_t cph = 0, aph = 0, sph = 0;
+        Unit u = blockIdx.x < nu ? A.units[blockIdx.x] : Unit{};
+        for (int ui = blockIdx.x; ui < nu; ui += grid) {
+            const Unit nx = next_unit(ui, u);
+            const int K = kdim(u), ng = K / G;
+            const bool ok = u.slot >= 0;
+            if (!ok && t == 0)
+                record_error(MOE_ERR_NOT_RESIDENT);
+            // the unit's scale rows -> (scale, bias) pairs [group][row]
+            if (!bar_wait(&s_full, sph))
+                s_dq_fail = 1;
+            sph ^= 1;
+            dq_sync(); // every dequant thread is done with the previous unit's pairs
+            if (s_dq_fail) {
+                s_abort = 1;
+                break;
             }
-            const int K = kdim(u);
-            const uint32_t *q;
-            const TS *sc, *bi;
-            if (A.mode == 0) { // interleaved: even rows gate, odd rows up, feature ft*64 + r/2
-                const int f = u.ft * 64 + (r >> 1);
-                const int m_q = (r & 1) ? M_QU : M_QG, m_s = (r & 1) ? M_SU : M_SG, m_b = (r & 1) ? M_BU : M_BG;
-                q = base ? reinterpret_cast<const uint32_t *>(base + off[m_q]) + (size_t)f * (K / 8) : nullptr;
-                sc = base ? reinterpret_cast<const TS *>(base + off[m_s]) + (size_t)f * (K / G) : nullptr;
-                bi = base ? reinterpret_cast<const TS *>(base + off[m_b]) + (size_t)f * (K / G) : nullptr;
-            } else {
-                const int h = u.ft * 128 + r;
-                q = base ? reinterpret_cast<const uint32_t *>(base + off[M_QD]) + (size_t)h * (K / 8) : nullptr;
-                sc = base ? reinterpret_cast<const TS *>(base + off[M_SD]) + (size_t)h * (K / G) : nullptr;
-                bi = base ? reinterpret_cast<const TS *>(base + off[M_BD]) + (size_t)h * (K / G) : nullptr;
+            {
+                const TS *raw = reinterpret_cast<const TS *>(s_raw);
+                for (int e = t; e < 128 * ng; e += kDqWarps * 32) {
+                    const int g = e >> 7, rr = e & 127;
+                    int si, bi;
+                    if (A.mode == 0) { // raw: sg, bg, su, bu, each [64 rows][ng]; rows interleave gate / up
+                        const int m = rr & 1, f = rr >> 1;
+                        si = (2 * m) * 64 * ng + f * ng + g;
+                        bi = si + 64 * ng;
+                    } else {           // raw: sd, bd, each [128 rows][ng]
+                        si = rr * ng + g;
+                        bi = si + 128 * ng;
+                    }
+                    s_pair[e] = SBPair<TS>{raw[si], raw[bi]};
+                }
             }
-            for (int k0 = 0; k0 < K; k0 += kBK) {
-                if (!bar_wait(&empty[stage], ph ^ 1)) {
+            dq_sync(); // the pairs are complete and the raw rows free
+            if (t == 0)
+                bar_arrive(&s_empty);
+            // this row's code piece (kCK / 2 bytes) in a code stage
+            const int coff = A.mode == 0 ? (r & 1) * (64 * kCK / 2) + (r >> 1) * (kCK / 2) : r * (kCK / 2);
+            bool wfail = false; // warp-uniform
+            for (int kc = 0; kc < K && !wfail; kc += kCK) {
+                if (!__all_sync(0xFFFFFFFFu, bar_wait(&c_full[cs], cph))) {
+                    s_dq_fail = 1;
                     s_abort = 1;
                     break;
                 }
-                unsigned char *tile = a_tiles + stage * kATile;
-                if (q) {
-                    dequant_row<TS>(q, sc, bi, k0, G, tile, r);
-                } else {
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4 *>(tile + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                const unsigned char *cp = c_ring + cs * kCTile + coff;
+                for (int k0 = kc; k0 < min(K, kc + kCK); k0 += kBK) {
+                    // warp-uniform, so that a give-up never splits the warp at __syncwarp
+                    if (!__all_sync(0xFFFFFFFFu, bar_wait(&ab_empty[as], aph ^ 1))) {
+                        s_dq_fail = 1;
+                        s_abort = 1;
+                        wfail = true;
+                        break;
+                    }
+                    unsigned char *row = a_tiles + as * kATile + r * 128;
+                    if (ok) {
+                        const uint2 qw = *reinterpret_cast<const uint2 *>(cp + (k0 - kc) / 2 + q * 8);
+                        const SBPair<TS> p = s_pair[((k0 + 16 * q) / G) * 128 + r];
+                        dequant_quarter(qw, to_f32(p.s), to_f32(p.b), row, r, q);
+                    } else {
+                        *reinterpret_cast<uint4 *>(row + (2 * q) * 16) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4 *>(row + (2 * q + 1) * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0)
+                        bar_arrive(&a_full[as]);
+                    if (++as == kStages) {
+                        as = 0;
+                        aph ^= 1;
+                    }
                 }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                bar_arrive(&a_full[stage]);
-                if (++stage == kStages) {
-                    stage = 0;
-                    ph ^= 1;
+                __syncwarp();
+                if (lane == 0)
+                    bar_arrive(&c_empty[cs]);
+                if (++cs == kCStages) {
+                    cs = 0;
+                    cph ^= 1;
                 }
             }
-            if (s_abort)
-                break;
+            u = nx;
         }
-    } else if (warp == 4) {
+    } else if (warp == kCodeWarp) {
+        // ---------------- TMA producer of the weight side: a unit's scale rows
+        // (issued as soon as the buffer is free, while the unit before is
+        // still in flight), then its code stages
+        if (lane == 0) {
+            int cs = 0;
+            uint32_t cph = 0, sph = 0;
+            int sui = blockIdx.x; // next unit whose scale rows are to be loaded
+            auto issue_scales = [&](const Unit &v) {
+                const CUtensorMap *mp = v.e < 0 ? wm.shared : wm.routed;
+                const int z = v.slot < 0 ? 0 : v.slot, ng = kdim(v) / G;
+                if (A.mode == 0) {
+                    const uint32_t part = 64u * (uint32_t)ng * sb;
+                    bar_expect(&s_full, 4 * part);
+                    for (int j = 0; j < 4; ++j) // sg bg su bu
+                        tma_load_3d(s_raw + j * part, &mp[2 + j], 0, v.ft * 64, z, &s_full);
+                } else {
+                    const uint32_t part = 128u * (uint32_t)ng * sb;
+                    bar_expect(&s_full, 2 * part);
+                    for (int j = 0; j < 2; ++j) // sd bd
+                        tma_load_3d(s_raw + j * part, &mp[1 + j], 0, v.ft * 128, z, &s_full);
+                }
+                sph ^= 1;
+                sui += grid;
+            };
+            Unit u = blockIdx.x < nu ? A.units[blockIdx.x] : Unit{};
+            for (int ui = blockIdx.x; ui < nu && !s_abort; ui += grid) {
+                const Unit nx = next_unit(ui, u);
+                if (sui == ui) { // this unit's scale rows: wait for the buffer
+                    if (!bar_wait(&s_empty, sph ^ 1)) {
+                        s_abort = 1;
+                        break;
+                    }
+                    issue_scales(u);
+                }
+                const int K = kdim(u);
+                const int z = u.slot < 0 ? 0 : u.slot;
+                const CUtensorMap *mp = u.e < 0 ? wm.shared : wm.routed;
+                for (int kc = 0; kc < K; kc += kCK) {
+                    if (sui == ui + grid && sui < nu && bar_try(&s_empty, sph ^ 1))
+                        issue_scales(nx);
+                    if (!bar_wait(&c_empty[cs], cph ^ 1)) {
+                        s_abort = 1;
+                        break;
+                    }
+                    // a piece past the row end (K not a multiple of kCK) is
+                    // zero-filled by the copy and never read
+                    unsigned char *cd = c_ring + cs * kCTile;
+                    bar_expect(&c_full[cs], kCTile);
+                    if (A.mode == 0) {
+                        tma_load_3d(cd, &mp[0], kc / 2, u.ft * 64, z, &c_full[cs]);
+                        tma_load_3d(cd + kCTile / 2, &mp[1], kc / 2, u.ft * 64, z, &c_full[cs]);
+                    } else {
+                        tma_load_3d(cd, &mp[0], kc / 2, u.ft * 128, z, &c_full[cs]);
+                    }
+                    if (++cs == kCStages) {
+                        cs = 0;
+                        cph ^= 1;
+                    }
+                }
+                u = nx;
+            }
+        }
+    } else if (warp == kRowWarp) {
         // ---------------- TMA producer for the token operand
         if (lane == 0) {
             int stage = 0;
             uint32_t ph = 0;
-            for (int ui = blockIdx.x; ui < nu && !s_abort; ui += gridDim.x) {
-                const Unit u = A.units[ui];
+            Unit u = blockIdx.x < nu ? A.units[blockIdx.x] : Unit{};
+            for (int ui = blockIdx.x; ui < nu && !s_abort; ui += grid) {
+                const Unit nx = next_unit(ui, u);
                 const int K = kdim(u);
                 const int nbox = (u.n + kBoxRows - 1) / kBoxRows;
                 // rows: gate/up routed -> sorted x; gate/up shared -> x; down -> activations
                 const CUtensorMap *map = (A.mode == 0 && u.e < 0) ? &tm_shared : &tm_rows;
                 const int row0 = (A.mode == 1 && u.e < 0) ? A.T * A.k + u.j0 : u.j0;
                 for (int k0 = 0; k0 < K; k0 += kBK) {
-                    if (!bar_wait(&empty[stage], ph ^ 1)) {
+                    if (!bar_wait(&ab_empty[stage], ph ^ 1)) {
                         s_abort = 1;
                         break;
                     }
@@ -431,15 +572,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ph ^= 1;
                     }
                 }
+                u = nx;
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kMmaWarp) {
         // ---------------- MMA issuer
         if (lane == 0) {
             int stage = 0, acc = 0;
             uint32_t ph = 0, acc_ph = 0;
-            for (int ui = blockIdx.x; ui < nu && !s_abort; ui += gridDim.x) {
-                const Unit u = A.units[ui];
+            Unit u = blockIdx.x < nu ? A.units[blockIdx.x] : Unit{};
+            for (int ui = blockIdx.x; ui < nu && !s_abort; ui += grid) {
+                const Unit nx = next_unit(ui, u);
                 const int K = kdim(u);
                 const int N = (u.n + 15) & ~15;
                 const uint32_t idesc = idesc_bf16(128, N);
@@ -461,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int kk = 0; kk < kBK / 16; ++kk)
                         mma_bf16(d_tmem, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32), idesc,
                                  (k0 > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(&empty[stage]);
+                    mma_commit(&ab_empty[stage]);
                     if (++stage == kStages) {
                         stage = 0;
                         ph ^= 1;
@@ -474,16 +617,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     acc = 0;
                     acc_ph ^= 1;
                 }
+                u = nx;
             }
         }
     } else {
-        // ---------------- epilogue: warps 6..9, TMEM lanes 32*(warp%4) ..
+        // ---------------- epilogue: 4 warps, TMEM lanes 32*(warp%4) ..
         const int quad = warp & 3;
         const int r = quad * 32 + lane; // tile row of this thread
         int acc = 0;
         uint32_t acc_ph = 0;
-        for (int ui = blockIdx.x; ui < nu && !s_abort; ui += gridDim.x) {
-            const Unit u = A.units[ui];
+        Unit u = blockIdx.x < nu ? A.units[blockIdx.x] : Unit{};
+        for (int ui = blockIdx.x; ui < nu && !s_abort; ui += grid) {
+            const Unit nx = next_unit(ui, u);
             if (!bar_wait(&acc_full[acc], acc_ph)) {
                 s_abort = 1;
                 break;
@@ -522,11 +667,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc = 0;
                 acc_ph ^= 1;
             }
+            u = nx;
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
     }
@@ -569,6 +715,56 @@ static bool make_map(CUtensorMap *m, const void *base, long rows, int cols)
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over one weight array of every slot of a pool: elements of a
+// row (inner), rows, slots; no swizzle.
+static bool make_wmap(CUtensorMap *m, CUtensorMapDataType dt, size_t esz, const char *base, uint64_t inner,
+                      uint64_t rows, uint64_t slots, uint64_t slot_stride, uint32_t box_inner, uint32_t box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[3] = {inner, rows, slots};
+    cuuint64_t strides[2] = {inner * esz, slot_stride};
+    cuuint32_t box[3] = {box_inner, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, dt, 3, const_cast<char *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+// The weight-side maps of one GEMM kind (mode 0 gate/up, 1 down), for the
+// routed pool and the shared blob.
+static bool make_wmaps(const Shape &s, const ExpertSrc &src, int mode, WMaps *w)
+{
+    const CUtensorMapDataType sdt = s.qscale == MOE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const size_t sb = s.qscale == MOE_F16 ? 2 : 4;
+    for (int side = 0; side < 2; ++side) {
+        const char *base = side ? src.shared : src.pool;
+        const size_t *off = side ? src.off_sh : src.off;
+        const uint64_t inter = side ? s.Is : s.I, slots = side ? 1 : src.n_slots;
+        const uint64_t stride = side ? (uint64_t)s.H * inter : src.stride; // one slot: any valid stride
+        CUtensorMap *m = side ? w->shared : w->routed;
+        bool ok;
+        if (mode == 0) {
+            ok = make_wmap(&m[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base + off[M_QG], s.H / 2, inter, slots, stride,
+                           kCK / 2, 64) &&
+                 make_wmap(&m[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base + off[M_QU], s.H / 2, inter, slots, stride,
+                           kCK / 2, 64);
+            const size_t so[4] = {off[M_SG], off[M_BG], off[M_SU], off[M_BU]};
+            for (int j = 0; ok && j < 4; ++j)
+                ok = make_wmap(&m[2 + j], sdt, sb, base + so[j], s.H / s.G, inter, slots, stride, s.H / s.G, 64);
+        } else {
+            ok = make_wmap(&m[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base + off[M_QD], inter / 2, s.H, slots, stride,
+                           kCK / 2, 128) &&
+                 make_wmap(&m[1], sdt, sb, base + off[M_SD], inter / s.G, s.H, slots, stride, inter / s.G, 128) &&
+                 make_wmap(&m[2], sdt, sb, base + off[M_BD], inter / s.G, s.H, slots, stride, inter / s.G, 128);
+        }
+        if (!ok)
+            return false;
+    }
+    return true;
+}
+
 static int sm_count()
 {
     int dev = 0, v = 0;
@@ -605,11 +801,30 @@ Layout layout(const Shape &s, int T)
     return L;
 }
 
+int min_tokens() { return kernel_path() == 2 ? 2 : kMinTokens; }
+
+bool wanted(const Shape &s, int T)
+{
+    if (kernel_path() == 1 || T < min_tokens() || T > 65536)
+        return false;
+    return s.act == MOE_BF16 && s.bits == 4 && s.H % 128 == 0 && s.I % 64 == 0 && s.Is % 64 == 0 && s.Is > 0;
+}
+
 bool eligible(const Shape &s, int T)
 {
-    if (kernel_path() != 0 || T < kMinTokens || T > 65536)
+    if (!wanted(s, T))
         return false;
-    if (s.act != MOE_BF16 || s.bits != 4 || s.H % 128 || s.I % 64 || s.Is % 64 || s.Is == 0)
+    // the weight-side staging: a half stage (32 K) in one group; a unit's
+    // scale and bias rows (16-byte rows, at most 256 elements) in one buffer
+    const int sb = s.qscale == MOE_F16 ? 2 : 4;
+    if (s.G % 32 || s.H / s.G > 256 || s.I / s.G > 256 || s.Is / s.G > 256)
+        return false;
+    if ((s.H / s.G * sb) % 16 || (s.I / s.G * sb) % 16 || (s.Is / s.G * sb) % 16)
+        return false;
+    if (256u * (s.H / s.G) * sb > kSTile || 256u * (s.I / s.G) * sb > kSTile || 256u * (s.Is / s.G) * sb > kSTile)
+        return false;
+    if (128u * 2 * sb * (s.H / s.G) > kPTile || 128u * 2 * sb * (s.I / s.G) > kPTile ||
+        128u * 2 * sb * (s.Is / s.G) > kPTile)
         return false;
     if (encode_fn() == nullptr)
         return false;
@@ -621,13 +836,14 @@ bool eligible(const Shape &s, int T)
 }
 
 template <typename TS>
-static cudaError_t gemm_go(const CUtensorMap &rows, const CUtensorMap &shared, const GemmArgs &g, cudaStream_t st)
+static cudaError_t gemm_go(const CUtensorMap &rows, const CUtensorMap &shared, const WMaps &wm, const GemmArgs &g,
+                           cudaStream_t st)
 {
     static int cur = 0;
     cudaError_t e = ensure_smem(grouped_gemm_kernel<TS>, kSmem, &cur);
     if (e != cudaSuccess)
         return e;
-    grouped_gemm_kernel<TS><<<sm_count(), kThreads, kSmem, st>>>(rows, shared, g);
+    grouped_gemm_kernel<TS><<<sm_count(), kThreads, kSmem, st>>>(rows, shared, wm, g);
     return cudaGetLastError();
 }
 
@@ -660,14 +876,17 @@ cudaError_t experts_forward(const Shape &s, const ExpertSrc &src, const void *x,
                                                       reinterpret_cast<uint4 *>(xs));
     pair_prep_kernel<<<(int)((P + T + 255) / 256), 256, 0, st>>>(perm_tok, perm_rank, topk_w, sg, T, s.k, wpair,
                                                                  inv);
-    plan_kernel<<<1, 1024, 0, st>>>(counts, offsets, s.E, T, s.I / 64, s.Is / 64, 1, u_gu, n_units);
-    plan_kernel<<<1, 1024, 0, st>>>(counts, offsets, s.E, T, s.H / 128, s.H / 128, 1, u_dn, n_units + 1);
+    plan_kernel<<<1, 1024, 0, st>>>(counts, offsets, src.table, src.n_slots, s.E, T, s.I / 64, s.Is / 64, 1, u_gu,
+                                    n_units);
+    plan_kernel<<<1, 1024, 0, st>>>(counts, offsets, src.table, src.n_slots, s.E, T, s.H / 128, s.H / 128, 1, u_dn,
+                                    n_units + 1);
     if ((e = cudaGetLastError()) != cudaSuccess)
         return e;
 
     CUtensorMap m_xs, m_x, m_act;
+    WMaps w_gu, w_dn;
     if (!make_map(&m_xs, xs, P + kNch, s.H) || !make_map(&m_x, x, T, s.H) ||
-        !make_map(&m_act, act, P + T + kNch, imax))
+        !make_map(&m_act, act, P + T + kNch, imax) || !make_wmaps(s, src, 0, &w_gu) || !make_wmaps(s, src, 1, &w_dn))
         return cudaErrorInvalidValue;
     GemmArgs g{};
     g.src = src;
@@ -684,13 +903,14 @@ cudaError_t experts_forward(const Shape &s, const ExpertSrc &src, const void *x,
     g.units = u_gu;
     g.n_units = n_units;
     g.mode = 0;
-    e = (s.qscale == MOE_F16) ? gemm_go<__half>(m_xs, m_x, g, st) : gemm_go<float>(m_xs, m_x, g, st);
+    e = (s.qscale == MOE_F16) ? gemm_go<__half>(m_xs, m_x, w_gu, g, st) : gemm_go<float>(m_xs, m_x, w_gu, g, st);
     if (e != cudaSuccess)
         return e;
     g.units = u_dn;
     g.n_units = n_units + 1;
     g.mode = 1;
-    e = (s.qscale == MOE_F16) ? gemm_go<__half>(m_act, m_act, g, st) : gemm_go<float>(m_act, m_act, g, st);
+    e = (s.qscale == MOE_F16) ? gemm_go<__half>(m_act, m_act, w_dn, g, st)
+                              : gemm_go<float>(m_act, m_act, w_dn, g, st);
     if (e != cudaSuccess)
         return e;
     combine_kernel<<<4 * sm_count(), 256, 0, st>>>(pout, inv, T, s.k, s.H, 1, static_cast<__nv_bfloat16 *>(y), y32);

@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kThreads) router_gemm_kernel(const __nv_bfloat
 bool router_gemm_eligible(const Shape &s, int T)
 {
     return T >= kRouterGemmMinTokens && s.act == MOE_BF16 && s.router == MOE_BF16 && s.H % rgemm::BK == 0 &&
-           kernel_path() == 0;
+           kernel_path() != 1;
 }
 
 cudaError_t launch_router_gemm(const Shape &s, const void *x, int T, const void *w_router, const float *bias,

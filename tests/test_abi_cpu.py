@@ -164,3 +164,25 @@ def test_noalloc_scratch_bound_stated_in_the_header():
     for shape in (synth.DEC_35B, synth.DEC_80B):
         cfg = B.config_for(shape)
         assert B.moe_layer_workspace_bytes(cfg, 63) <= 4 << 20 < B.moe_layer_workspace_bytes(cfg, 64)
+
+
+def test_kernel_path_values_and_workspace_follow_the_path():
+    """Paths 0, 1, 2 are accepted (per thread), others refused; the grouped-GEMM
+    buffers join the workspace from T = 2 under path 2 only."""
+    cfg = B.config_for(synth.DEC_80B)
+    try:
+        for bad in (-1, 3):
+            with pytest.raises(B.MoEError) as ei:
+                B.moe_set_kernel_path(bad)
+            assert ei.value.status == B.MOE_ERR_INVALID_ARG
+        sizes = {}
+        for p in (0, 1, 2):
+            B.moe_set_kernel_path(p)
+            sizes[p] = B.moe_layer_workspace_bytes(cfg, 8)
+        assert sizes[0] == sizes[1] < sizes[2]
+        B.moe_set_kernel_path(0)
+        one = B.moe_layer_workspace_bytes(cfg, 1)
+        B.moe_set_kernel_path(2)
+        assert B.moe_layer_workspace_bytes(cfg, 1) == one      # T = 1 stays on the single-token kernels
+    finally:
+        B.moe_set_kernel_path(0)
