@@ -295,7 +295,9 @@ typedef struct {
 /* One layer of a pooled stack, end to end: route x on `stream`, read the
  * top-k ids back to the host (the one synchronisation of `stream`), apply the
  * pool policy, fill the misses on the pool's side stream, make `stream` wait
- * for the fills, then run the experts from the pool.  T tokens; their
+ * for the fills, then run the experts from the pool.  A pool in device mode
+ * (slot_pool_enable_device) does the lookup and fills as kernels on `stream`
+ * instead, with no synchronisation.  T tokens; their
  * distinct experts must fit the layer's slots (MOE_ERR_POOL_EXHAUSTED
  * otherwise).  x, y, y_f32 (nullable), topk_idx_out (nullable) and workspace
  * (moe_layer_workspace_bytes) are device pointers. */
@@ -303,6 +305,28 @@ moe_status moe_pooled_layer_forward(const moe_config *cfg, slot_pool *p, int32_t
                                     const moe_resident_weights *w, const void *x, int32_t T, void *y,
                                     float *y_f32, int32_t *topk_idx_out, void *workspace,
                                     size_t ws_bytes, cudaStream_t stream);
+
+/* Device-side policy.  slot_pool_enable_device switches a pool that has
+ * served no host lookup to running its rule on the device: the same rule,
+ * the same tie breaks and the same clock as slot_pool_lookup, kept in device
+ * copies of the use counts, stamps and slot owners.  Its fills are read by a
+ * kernel straight from the backing store, which must then be pinned host
+ * memory the device can address (MOE_ERR_UNSUPPORTED otherwise); at most
+ * 2048 slots per layer.  From then on the host lookup and fill calls are
+ * refused, slot_pool_table_host and slot_pool_stats copy from the device
+ * (exposed_copy_ns stays 0), and moe_pooled_layer_forward enqueues route,
+ * lookup, fills and experts on its stream with no host synchronisation, so
+ * a stack of layers can be captured in one CUDA graph.  Device-mode calls on
+ * one pool must be ordered (one stream, or events between streams).
+ *
+ * slot_pool_step_device: one lookup of the n expert ids at ids_dev (device)
+ * for `layer`, and the fills it needs, enqueued on `stream`.  Bad ids record
+ * MOE_ERR_DEVICE_FAULT, more distinct ids than slots MOE_ERR_POOL_EXHAUSTED,
+ * in the device error word (moe_get_device_error); the lookup is then
+ * skipped. */
+moe_status slot_pool_enable_device(slot_pool *p);
+moe_status slot_pool_step_device(slot_pool *p, int32_t layer, const int32_t *ids_dev, int32_t n,
+                                 cudaStream_t stream);
 
 moe_status slot_pool_stats(slot_pool *p, moe_pool_stats *out);
 void slot_pool_destroy(slot_pool *p);

@@ -100,6 +100,8 @@ _SIGS = {
                                       _P, _Z, _P]),
     "slot_pool_destroy": (None, [_P]),
     "slot_pool_set_policy": (_I, [_P, _I]),
+    "slot_pool_enable_device": (_I, [_P]),
+    "slot_pool_step_device": (_I, [_P, _I, _P, _I, _P]),
     "moe_get_device_error": (_I, [_P]),
     "moe_last_error_message": (C.c_char_p, []),
     "moe_version": (C.c_char_p, []),
@@ -285,6 +287,14 @@ MOE_POOL_LFU_RECENCY, MOE_POOL_LRU, MOE_POOL_LFU = 0, 1, 2
 
 def slot_pool_set_policy(pool: int, policy: int) -> None:
     _check(lib().slot_pool_set_policy(pool, policy), "slot_pool_set_policy")
+
+
+def slot_pool_enable_device(pool: int) -> None:
+    _check(lib().slot_pool_enable_device(pool), "slot_pool_enable_device")
+
+
+def slot_pool_step_device(pool: int, layer: int, ids_dev, n: int, stream=None) -> None:
+    _check(lib().slot_pool_step_device(pool, layer, _ptr(ids_dev), n, _stream(stream)), "slot_pool_step_device")
 
 
 def slot_pool_destroy(pool: int) -> None:

@@ -43,6 +43,174 @@ struct Fill {
     int32_t expert, slot, evicted;
 };
 
+enum { C_CLOCK = 0, C_LOOKUPS, C_HITS, C_MISSES, C_EVICTIONS, C_BYTES, C_N };
+
+constexpr int kLookupThreads = 256;
+constexpr int kMaxUniq = 1024; // distinct experts one device lookup takes
+
+// Victim key of the device lookup, compared lexicographically.
+struct VKey {
+    int cls;
+    long long a, b;
+    int slot;
+    __device__ bool less(const VKey &o) const
+    {
+        if (cls != o.cls)
+            return cls < o.cls;
+        if (a != o.a)
+            return a < o.a;
+        if (b != o.b)
+            return b < o.b;
+        return slot < o.slot;
+    }
+};
+
+// The pool rule on one layer's device state, for the n expert ids at ids
+// (device): the same steps, in the same order, as slot_pool_lookup on the
+// host.  Distinct ids in order of first appearance; hits are counted and
+// stamped; each miss takes the lowest empty slot, else the slot whose expert
+// the lookup does not need with the smallest key (policy), ties to the lowest
+// slot id.  The (expert, slot) pairs to fill go to fills (count first).  One
+// CTA.
+__global__ void __launch_bounds__(kLookupThreads) pool_lookup_kernel(const int32_t *__restrict__ ids, int n, int E,
+                                                                     int S, int policy, int32_t *__restrict__ table,
+                                                                     int32_t *__restrict__ owner,
+                                                                     long long *__restrict__ freq,
+                                                                     long long *__restrict__ stamp,
+                                                                     long long *__restrict__ ctr,
+                                                                     int32_t *__restrict__ fills, long long blob_bytes)
+{
+    __shared__ int32_t uniq[kMaxUniq], miss[kMaxUniq];
+    __shared__ int n_uniq, n_miss, bad;
+    __shared__ long long clock;
+    __shared__ VKey wbest[kLookupThreads / 32];
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    if (t == 0) {
+        int nu = 0, b = 0;
+        for (int j = 0; j < n && !b; ++j) {
+            const int e = ids[j];
+            if (e < 0 || e >= E) {
+                b = MOE_ERR_DEVICE_FAULT;
+                break;
+            }
+            bool seen = false;
+            for (int u = 0; u < nu; ++u)
+                seen |= uniq[u] == e;
+            if (!seen) {
+                if (nu == S || nu == kMaxUniq) {
+                    b = MOE_ERR_POOL_EXHAUSTED;
+                    break;
+                }
+                uniq[nu++] = e;
+            }
+        }
+        bad = b;
+        n_uniq = nu;
+        fills[0] = 0;
+        if (!b) {
+            clock = ++ctr[C_CLOCK];
+            ctr[C_LOOKUPS] += 1;
+            int nm = 0;
+            for (int u = 0; u < nu; ++u) {
+                const int e = uniq[u], sl = table[e];
+                if (sl >= 0) {
+                    freq[sl] += 1;
+                    stamp[sl] = clock;
+                    ctr[C_HITS] += 1;
+                } else {
+                    miss[nm++] = e;
+                }
+            }
+            n_miss = nm;
+        } else {
+            n_miss = 0;
+        }
+    }
+    __syncthreads();
+    if (bad) {
+        if (t == 0)
+            moe::record_error(bad);
+        return;
+    }
+    const int nu = n_uniq, nm = n_miss;
+    for (int m = 0; m < nm; ++m) {
+        // victim search: key (class, a, b, slot), smallest first; class 0 =
+        // empty slot, 1 = a slot whose expert this lookup does not need,
+        // 2 = not a candidate; (a, b) = (use count, stamp) under LFU +
+        // recency, (stamp, 0) under LRU, (use count, 0) under LFU
+        VKey best{2, 0, 0, 0x7FFFFFFF};
+        for (int j = t; j < S; j += kLookupThreads) {
+            const int o = owner[j];
+            VKey kj{0, 0, 0, j};
+            if (o >= 0) {
+                bool needed = false;
+                for (int u = 0; u < nu; ++u)
+                    needed |= uniq[u] == o;
+                kj.cls = needed ? 2 : 1;
+                kj.a = policy == MOE_POOL_LRU ? stamp[j] : freq[j];
+                kj.b = policy == MOE_POOL_LFU_RECENCY ? stamp[j] : 0;
+            }
+            if (kj.less(best))
+                best = kj;
+        }
+        for (int o = 16; o > 0; o >>= 1) {
+            VKey v{__shfl_xor_sync(0xFFFFFFFFu, best.cls, o), __shfl_xor_sync(0xFFFFFFFFu, best.a, o),
+                   __shfl_xor_sync(0xFFFFFFFFu, best.b, o), __shfl_xor_sync(0xFFFFFFFFu, best.slot, o)};
+            if (v.less(best))
+                best = v;
+        }
+        if (lane == 0)
+            wbest[warp] = best;
+        __syncthreads();
+        if (t == 0) {
+            for (int w = 1; w < kLookupThreads / 32; ++w)
+                if (wbest[w].less(best))
+                    best = wbest[w];
+            if (best.cls == 2) { // cannot happen with n_uniq <= S
+                moe::record_error(MOE_ERR_DEVICE_FAULT);
+                n_miss = m;
+                break;
+            }
+            const int sl = best.slot;
+            const int e = miss[m], ev = owner[sl];
+            if (ev >= 0) {
+                table[ev] = -1;
+                ctr[C_EVICTIONS] += 1;
+            }
+            owner[sl] = e;
+            table[e] = sl;
+            freq[sl] = 1;
+            stamp[sl] = clock;
+            ctr[C_MISSES] += 1;
+            ctr[C_BYTES] += blob_bytes;
+            fills[1 + 2 * m] = e;
+            fills[2 + 2 * m] = sl;
+        }
+        __syncthreads();
+    }
+    if (t == 0)
+        fills[0] = nm;
+}
+
+// Copy the blobs of the last lookup's fills from the backing store (host
+// memory the device reads through the mapping) into their slots: 16-byte
+// pieces, grid-stride over (fill, piece).
+__global__ void __launch_bounds__(256) pool_fill_kernel(const int32_t *__restrict__ fills, const char *backing,
+                                                        char *__restrict__ pool, size_t stride, size_t blob_bytes,
+                                                        int E)
+{
+    const int nf = fills[0];
+    const size_t per = blob_bytes / 16;
+    const size_t total = (size_t)nf * per;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        const int f = (int)(i / per);
+        const size_t c = i - (size_t)f * per;
+        const int e = fills[1 + 2 * f], sl = fills[2 + 2 * f];
+        reinterpret_cast<uint4 *>(pool + (size_t)sl * stride)[c] =
+            __ldcs(reinterpret_cast<const uint4 *>(backing + (size_t)e * stride) + c);
+    }
+}
+
 } // namespace
 
 struct slot_pool {
@@ -68,6 +236,14 @@ struct slot_pool {
     std::vector<int32_t> tmp_slots, tmp_miss;
     cudaEvent_t fill_done = nullptr, wait_begin = nullptr, wait_end = nullptr;
     bool pending_exposure = false;
+    // device-side policy (slot_pool_enable_device): the same rule on device
+    // copies of the policy state, fills read from the mapped backing store
+    bool device_mode = false;
+    const char *backing_dev = nullptr;
+    int32_t *d_owner = nullptr;            // [L*S]
+    long long *d_freq = nullptr, *d_stamp = nullptr; // [L*S]
+    long long *d_ctr = nullptr;            // clock, lookups, hits, misses, evictions, bytes_filled
+    int32_t *d_fills = nullptr;            // [L][1 + 2*S]: count, then (expert, slot) pairs of the last lookup
 };
 
 extern "C" moe_status slot_pool_create(const moe_config *cfg, int32_t n_layers, int32_t slots_per_layer,
@@ -148,6 +324,8 @@ extern "C" moe_status slot_pool_lookup(slot_pool *p, int32_t layer, const int32_
     if (layer < 0 || layer >= p->L || n < 0)
         return fail(MOE_ERR_INVALID_ARG, "slot_pool_lookup: layer %d or n %d out of range", layer, n);
     std::lock_guard<std::mutex> g(p->mu);
+    if (p->device_mode)
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_lookup: the pool runs its policy on the device");
     const int E = p->s.E, S = p->S;
     std::vector<int32_t> uniq;
     for (int j = 0; j < n; ++j) {
@@ -315,6 +493,10 @@ extern "C" moe_status slot_pool_table_host(slot_pool *p, int32_t layer, int32_t 
     if (layer < 0 || layer >= p->L)
         return fail(MOE_ERR_INVALID_ARG, "slot_pool_table_host: layer %d out of range", layer);
     std::lock_guard<std::mutex> g(p->mu);
+    if (p->device_mode)
+        return cuda_check(cudaMemcpy(table_host, p->table_dev + (size_t)layer * p->s.E, sizeof(int32_t) * p->s.E,
+                                     cudaMemcpyDeviceToHost),
+                          "slot_pool_table_host: device table");
     for (int e = 0; e < p->s.E; ++e)
         table_host[e] = p->table[(size_t)layer * p->s.E + e];
     return MOE_OK;
@@ -332,12 +514,22 @@ static void harvest_exposure(slot_pool *p)
     p->pending_exposure = false;
 }
 
+static moe_status device_step(slot_pool *p, int32_t layer, const int32_t *ids_dev, int32_t n, cudaStream_t stream);
+
 extern "C" moe_status slot_pool_stats(slot_pool *p, moe_pool_stats *out)
 {
     using namespace moe;
     if (!p || !out)
         return fail(MOE_ERR_INVALID_ARG, "slot_pool_stats: NULL argument");
     std::lock_guard<std::mutex> g(p->mu);
+    if (p->device_mode) {
+        long long c[C_N];
+        cudaError_t e = cudaMemcpy(c, p->d_ctr, sizeof(c), cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess)
+            return cuda_check(e, "slot_pool_stats: device counters");
+        *out = moe_pool_stats{c[C_LOOKUPS], c[C_HITS], c[C_MISSES], c[C_EVICTIONS], c[C_BYTES], 0};
+        return MOE_OK;
+    }
     harvest_exposure(p);
     *out = p->st;
     return MOE_OK;
@@ -379,6 +571,15 @@ extern "C" moe_status moe_pooled_layer_forward(const moe_config *cfg, slot_pool 
         return st;
 
     const size_t n_ids = (size_t)T * s.k;
+    if (p->device_mode) {
+        // no host round trip: lookup and fills are kernels on `stream`
+        st = device_step(p, layer, idx, (int32_t)n_ids, stream);
+        if (st != MOE_OK)
+            return st;
+        moe_layer L{w->w_router, w->router_bias, w->w_shared_gate, w->shared_blob,
+                    p->pool + (size_t)layer * p->S * p->stride, p->stride, p->table_dev + (size_t)layer * s.E, p->S};
+        return moe_experts_forward(cfg, &L, x, T, idx, tw, sg, y, y_f32, workspace, ws_bytes, stream);
+    }
     {
         std::lock_guard<std::mutex> g(p->mu);
         moe_status ts = ensure_table_dev(p);
@@ -438,6 +639,93 @@ extern "C" moe_status moe_pooled_layer_forward(const moe_config *cfg, slot_pool 
     return moe_experts_forward(cfg, &L, x, T, idx, tw, sg, y, y_f32, workspace, ws_bytes, stream);
 }
 
+// ------------------------------------------------------------ device-side policy
+
+extern "C" moe_status slot_pool_enable_device(slot_pool *p)
+{
+    using namespace moe;
+    if (!p)
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_enable_device: NULL pool");
+    std::lock_guard<std::mutex> g(p->mu);
+    if (p->device_mode)
+        return MOE_OK;
+    if (p->st.lookups != 0)
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_enable_device: the pool has already served host lookups");
+    if (p->S > kMaxUniq * 2)
+        return fail(MOE_ERR_UNSUPPORTED, "slot_pool_enable_device: %d slots per layer (at most %d)", p->S,
+                    kMaxUniq * 2);
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p->backing) != cudaSuccess || at.type != cudaMemoryTypeHost ||
+        !at.devicePointer) {
+        cudaGetLastError();
+        return fail(MOE_ERR_UNSUPPORTED, "slot_pool_enable_device: the backing store is not pinned host memory "
+                                         "the device can read");
+    }
+    moe_status ts = ensure_table_dev(p);
+    if (ts != MOE_OK)
+        return ts;
+    const size_t LS = (size_t)p->L * p->S;
+    cudaError_t e = cudaMalloc(&p->d_owner, LS * sizeof(int32_t));
+    if (e == cudaSuccess)
+        e = cudaMalloc(&p->d_freq, LS * sizeof(long long));
+    if (e == cudaSuccess)
+        e = cudaMalloc(&p->d_stamp, LS * sizeof(long long));
+    if (e == cudaSuccess)
+        e = cudaMalloc(&p->d_ctr, C_N * sizeof(long long));
+    if (e == cudaSuccess)
+        e = cudaMalloc(&p->d_fills, (size_t)p->L * (1 + 2 * (size_t)p->S) * sizeof(int32_t));
+    if (e == cudaSuccess)
+        e = cudaMemset(p->d_owner, 0xFF, LS * sizeof(int32_t));
+    if (e == cudaSuccess)
+        e = cudaMemset(p->d_freq, 0, LS * sizeof(long long));
+    if (e == cudaSuccess)
+        e = cudaMemset(p->d_stamp, 0, LS * sizeof(long long));
+    if (e == cudaSuccess)
+        e = cudaMemset(p->d_ctr, 0, C_N * sizeof(long long));
+    if (e == cudaSuccess)
+        e = cudaMemset(p->d_fills, 0, (size_t)p->L * (1 + 2 * (size_t)p->S) * sizeof(int32_t));
+    if (e == cudaSuccess)
+        e = cudaDeviceSynchronize();
+    if (e != cudaSuccess)
+        return cuda_check(e, "slot_pool_enable_device: device state");
+    p->backing_dev = static_cast<const char *>(at.devicePointer);
+    p->device_mode = true;
+    return MOE_OK;
+}
+
+// Lookup + fills of one layer on `stream` (device mode; the caller holds no lock).
+static moe_status device_step(slot_pool *p, int32_t layer, const int32_t *ids_dev, int32_t n, cudaStream_t stream)
+{
+    using namespace moe;
+    const int E = p->s.E, S = p->S;
+    int32_t *fills = p->d_fills + (size_t)layer * (1 + 2 * (size_t)S);
+    pool_lookup_kernel<<<1, kLookupThreads, 0, stream>>>(
+        ids_dev, n, E, S, p->policy, p->table_dev + (size_t)layer * E, p->d_owner + (size_t)layer * S,
+        p->d_freq + (size_t)layer * S, p->d_stamp + (size_t)layer * S, p->d_ctr, fills, (long long)p->blob_bytes);
+    int sms = 0, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    pool_fill_kernel<<<4 * (sms > 0 ? sms : 148), 256, 0, stream>>>(
+        fills, p->backing_dev + (size_t)layer * E * p->stride, p->pool + (size_t)layer * S * p->stride, p->stride,
+        p->blob_bytes, E);
+    return cuda_check(cudaGetLastError(), "slot pool device step");
+}
+
+extern "C" moe_status slot_pool_step_device(slot_pool *p, int32_t layer, const int32_t *ids_dev, int32_t n,
+                                            cudaStream_t stream)
+{
+    using namespace moe;
+    if (!p || (n > 0 && !ids_dev))
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_step_device: NULL argument");
+    if (!p->device_mode)
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_step_device: the pool is not in device mode");
+    if (layer < 0 || layer >= p->L || n < 0 || n > 65535 * 16)
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_step_device: layer %d or n %d out of range", layer, n);
+    if (n == 0)
+        return MOE_OK;
+    return device_step(p, layer, ids_dev, n, stream);
+}
+
 extern "C" void slot_pool_destroy(slot_pool *p)
 {
     if (!p)
@@ -446,6 +734,9 @@ extern "C" void slot_pool_destroy(slot_pool *p)
         cudaEventSynchronize(p->wait_end);
     if (p->table_dev)
         cudaFree(p->table_dev);
+    for (void *d : {(void *)p->d_owner, (void *)p->d_freq, (void *)p->d_stamp, (void *)p->d_ctr, (void *)p->d_fills})
+        if (d)
+            cudaFree(d);
     if (p->pinned_ids)
         cudaFreeHost(p->pinned_ids);
     if (p->fill_done)

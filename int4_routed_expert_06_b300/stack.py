@@ -5,7 +5,8 @@ layer's expert blobs at a fixed stride, the device pool buffer, the resident
 part of each layer (router, shared gate, shared expert) and the side stream
 fills run on.  Each layer step is one ``moe_pooled_layer_forward`` call; the
 routing, the LFU+recency policy, the fills and the expert kernels all run in
-the library.
+the library, the policy on the host, or (device_policy=True) as kernels on
+the caller's stream, with the fills read from the pinned backing store.
 """
 from __future__ import annotations
 
@@ -18,7 +19,8 @@ from . import binding as B
 
 class PooledStack:
     def __init__(self, shape, n_layers: int, slots_per_layer: int,
-                 layer_weights: Callable[[int], Dict[str, torch.Tensor]], device: str = "cuda"):
+                 layer_weights: Callable[[int], Dict[str, torch.Tensor]], device: str = "cuda",
+                 device_policy: bool = False):
         self.shape, self.cfg = shape, B.config_for(shape)
         self.L, self.S, self.E = n_layers, slots_per_layer, shape.n_experts
         lay = B.moe_blob_layout_get(self.cfg, shape.inter)
@@ -46,6 +48,9 @@ class PooledStack:
         self.side = torch.cuda.Stream()
         self.handle = B.slot_pool_create(self.cfg, n_layers, slots_per_layer, self.pool, self.pool.numel(),
                                          self.backing, self.stride, self.side)
+        self.device_policy = device_policy
+        if device_policy:  # lookup and fills as kernels on the caller's stream: no host round trip
+            B.slot_pool_enable_device(self.handle)
         self.ws_bytes = 0
         self.ws = None
 

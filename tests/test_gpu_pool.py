@@ -29,9 +29,14 @@ SHAPE = dataclasses.replace(synth.STACK_80B, name="pool-test", n_experts=64, top
 
 
 @pytest.fixture(scope="module")
-def stack():
-    weights = [synth.make_layer(SHAPE, seed=40 + l, device="cuda") for l in range(SHAPE.layers)]
-    st = PooledStack(SHAPE, SHAPE.layers, SHAPE.pool_slots, lambda l: weights[l])
+def weights():
+    return [synth.make_layer(SHAPE, seed=40 + l, device="cuda") for l in range(SHAPE.layers)]
+
+
+@pytest.fixture(scope="module", params=["host", "device"])
+def stack(request, weights):
+    st = PooledStack(SHAPE, SHAPE.layers, SHAPE.pool_slots, lambda l: weights[l],
+                     device_policy=request.param == "device")
     resident = [B.DeviceLayer(SHAPE, weights[l], torch.arange(SHAPE.n_experts, dtype=torch.int32))
                 for l in range(SHAPE.layers)]
     yield st, weights, resident
@@ -39,6 +44,7 @@ def stack():
 
 
 def test_pool_stack_bit_identical_to_resident_and_policy_exact(stack):
+    """Host and device policy: the same outputs, tables and counters."""
     st, weights, resident = stack
     L, E, k = SHAPE.layers, SHAPE.n_experts, SHAPE.top_k
     policy = SlotPolicy(L, E, SHAPE.pool_slots)
@@ -79,7 +85,8 @@ def test_pool_stack_bit_identical_to_resident_and_policy_exact(stack):
     s = st.stats()
     assert (s["hits"], s["misses"], s["evictions"]) == (policy.hits, policy.misses, policy.evictions)
     assert s["bytes_filled"] == policy.misses * st.blob_bytes
-    assert s["exposed_copy_ns"] > 0 and s["lookups"] == 24 * L
+    assert s["lookups"] == 24 * L
+    assert (s["exposed_copy_ns"] > 0) == (not st.device_policy)
     assert policy.hits > 0 and policy.evictions > 0
 
 
@@ -97,3 +104,93 @@ def test_pool_exhaustion_is_an_error_not_a_fault(stack):
         assert B.moe_get_device_error() == 0
     finally:
         p.close()
+
+
+def test_device_policy_stack_in_one_cuda_graph(weights):
+    """Device mode has no host round trip: several tokens through every
+    layer, captured once and replayed, stay bit-identical to the resident
+    layers, and the pool counters advance by one lookup per layer-token."""
+    L, E, k = SHAPE.layers, SHAPE.n_experts, SHAPE.top_k
+    st = PooledStack(SHAPE, L, SHAPE.pool_slots, lambda l: weights[l], device_policy=True)
+    resident = [B.DeviceLayer(SHAPE, weights[l], torch.arange(E, dtype=torch.int32)) for l in range(L)]
+    try:
+        n_tok = 6
+        x0 = synth.decode_xs(SHAPE, n_tok, seed0=synth.STACK_X_SEED0 + 100, device="cuda")
+        Y = torch.empty((n_tok, L, SHAPE.hidden), dtype=torch.bfloat16, device="cuda")
+        stream = torch.cuda.Stream()
+        st.workspace(1)
+
+        def run():
+            for j in range(n_tok):
+                h = x0[j:j + 1]
+                for l in range(L):
+                    st.layer_forward(l, layer_input(h), Y[j, l:l + 1], stream=stream)
+                    h = (h.float() + Y[j, l:l + 1].float()).to(torch.bfloat16)
+
+        with torch.cuda.stream(stream):
+            run()                                     # eager once: kernel attributes before capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            run()
+        s0 = st.stats()
+        for _ in range(3):
+            Y.zero_()
+            with torch.cuda.stream(stream):
+                g.replay()
+            torch.cuda.synchronize()
+            assert B.moe_get_device_error() == 0
+            nb = B.moe_layer_workspace_bytes(st.cfg, 1)
+            ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+            yr = torch.empty((1, SHAPE.hidden), dtype=torch.bfloat16, device="cuda")
+            for j in range(n_tok):
+                h = x0[j:j + 1]
+                for l in range(L):
+                    B.moe_layer_forward(st.cfg, resident[l].struct(), layer_input(h), 1, yr, None, None, None, ws, nb)
+                    torch.cuda.synchronize()
+                    assert torch.equal(yr, Y[j, l:l + 1]), (j, l)
+                    h = (h.float() + yr.float()).to(torch.bfloat16)
+        s1 = st.stats()
+        assert s1["lookups"] - s0["lookups"] == 3 * n_tok * L
+        assert s1["hits"] + s1["misses"] > s0["hits"] + s0["misses"]
+    finally:
+        st.close()
+
+
+def test_device_step_bad_ids_recorded_not_faulted(weights):
+    st = PooledStack(SHAPE, 1, 4, lambda l: weights[0], device_policy=True)
+    try:
+        bad = torch.tensor([3, SHAPE.n_experts + 5], dtype=torch.int32, device="cuda")
+        B.slot_pool_step_device(st.handle, 0, bad, 2)
+        torch.cuda.synchronize()
+        assert B.moe_get_device_error() == B.MOE_ERR_DEVICE_FAULT
+        many = torch.arange(8, dtype=torch.int32, device="cuda")   # 8 distinct, 4 slots
+        B.slot_pool_step_device(st.handle, 0, many, 8)
+        torch.cuda.synchronize()
+        assert B.moe_get_device_error() == B.MOE_ERR_POOL_EXHAUSTED
+        assert B.slot_pool_table_host(st.handle, 0, SHAPE.n_experts) == [-1] * SHAPE.n_experts
+        ok = torch.tensor([5, 9, 5], dtype=torch.int32, device="cuda")
+        B.slot_pool_step_device(st.handle, 0, ok, 3)
+        torch.cuda.synchronize()
+        assert B.moe_get_device_error() == 0
+        t = B.slot_pool_table_host(st.handle, 0, SHAPE.n_experts)
+        assert (t[5], t[9]) == (0, 1) and sum(v >= 0 for v in t) == 2
+        with pytest.raises(B.MoEError):
+            B.slot_pool_lookup(st.handle, 0, [1, 2])      # host lookups refused in device mode
+    finally:
+        st.close()
+
+
+def test_device_policy_needs_a_device_readable_backing_store():
+    cfg = B.config_for(SHAPE)
+    lay = B.moe_blob_layout_get(cfg, SHAPE.inter)
+    stride = (lay.bytes + 255) // 256 * 256
+    pool = torch.empty(stride * 4, dtype=torch.uint8, device="cuda")
+    pageable = torch.empty(stride * SHAPE.n_experts, dtype=torch.uint8)     # not pinned
+    h = B.slot_pool_create(cfg, 1, 4, pool, pool.numel(), pageable, stride, None)
+    try:
+        with pytest.raises(B.MoEError) as ei:
+            B.slot_pool_enable_device(h)
+        assert ei.value.status == B.MOE_ERR_UNSUPPORTED
+    finally:
+        B.slot_pool_destroy(h)
