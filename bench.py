@@ -26,7 +26,11 @@ at batch 1); no collective touches the data path.
 `--workload 35b-dec`, `80b-dec-int8` and `35b-dec-int8` time the same decode
 loop on the 35B-shaped layer and on both layers with affine int8 codes.
 
-Three more workloads print their own line (not the default):
+Four more workloads print their own line (not the default):
+
+- `--workload 80b-pool-sweep`: tokens/s and hit rate of an 8-layer stack
+  through the bounded pool (device-side policy) against pool size and
+  routing skew, beside the all-resident stack.
 
 - `--workload 80b-batch`: tokens/s of one 80B-shaped layer call of T = 1 ..
   64 tokens on each kernel path (generic kernels, tcgen05 grouped GEMMs, and
@@ -45,6 +49,7 @@ Three more workloads print their own line (not the default):
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -436,56 +441,78 @@ def run_stack(args, shape):
         return w
 
     t_build = time.perf_counter()
-    st = PooledStack(shape, L, shape.pool_slots, weights)
+    st = PooledStack(shape, L, shape.pool_slots, weights, device_policy=True)
     t_build = time.perf_counter() - t_build
     n = args.warmup + args.steps
     x0 = synth.decode_xs(shape, n, seed0=synth.STACK_X_SEED0, device="cuda")
     Y = torch.empty((n, L, shape.hidden), dtype=torch.bfloat16, device="cuda")
-    stream = torch.cuda.current_stream()
+    stream = torch.cuda.Stream()
+    st.workspace(1)
 
     def token(j):
         h = x0[j:j + 1]
         for l in range(L):
-            st.layer_forward(l, layer_input(h), Y[j, l:l + 1])
+            st.layer_forward(l, layer_input(h), Y[j, l:l + 1], stream=stream)
             h = (h.float() + Y[j, l:l + 1].float()).to(torch.bfloat16)
 
-    for j in range(args.warmup):
-        token(j)
+    with torch.cuda.stream(stream):
+        for j in range(args.warmup):  # eager: fills the pool, sets kernel attributes
+            token(j)
+    torch.cuda.synchronize()
+    # the timed tokens, every layer of each, as one CUDA graph: the pool's
+    # lookups and fills are kernels, so nothing waits on the host
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for j in range(args.warmup, n):
+            token(j)
     torch.cuda.synchronize()
     s0 = st.stats()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(0) as clk:
         t_wall = time.perf_counter()
-        start.record(stream)
-        for j in range(args.warmup, n):
-            token(j)
-        end.record(stream)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            graph.replay()
+            end.record(stream)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
     ms = start.elapsed_time(end)
     s1 = st.stats()
     if B.moe_get_device_error() != 0:
         raise RuntimeError("a kernel recorded a device error during the bench")
-    d = {key: s1[key] - s0[key] for key in ("hits", "misses", "evictions", "bytes_filled", "exposed_copy_ns",
-                                             "lookups")}
-    # the same tokens through all-resident layers: timing, and bit-identity of every layer output
+    del graph
+    d = {key: s1[key] - s0[key] for key in ("hits", "misses", "evictions", "bytes_filled", "lookups")}
+    # the same tokens through all-resident layers, also one graph: timing, and
+    # bit-identity of every layer output
     cfg = st.cfg
     nb = B.moe_layer_workspace_bytes(cfg, 1)
     ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
-    yr = torch.empty((1, shape.hidden), dtype=torch.bfloat16, device="cuda")
-    mism = torch.zeros((), dtype=torch.int64, device="cuda")
-    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    r0.record(stream)
-    for j in range(args.warmup, n):
+    YR = torch.empty_like(Y)
+
+    def token_resident(j):
         h = x0[j:j + 1]
         for l in range(L):
-            B.moe_layer_forward(cfg, resident[l].struct(), layer_input(h), 1, yr, None, None, None, ws, nb)
-            mism += (yr != Y[j, l:l + 1]).any()
-            h = (h.float() + yr.float()).to(torch.bfloat16)
-    r1.record(stream)
+            B.moe_layer_forward(cfg, resident[l].struct(), layer_input(h), 1, YR[j, l:l + 1], None, None, None,
+                                ws, nb, stream)
+            h = (h.float() + YR[j, l:l + 1].float()).to(torch.bfloat16)
+
+    with torch.cuda.stream(stream):
+        token_resident(0)
+    torch.cuda.synchronize()
+    graph_r = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_r, stream=stream):
+        for j in range(args.warmup, n):
+            token_resident(j)
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        r0.record(stream)
+        graph_r.replay()
+        r1.record(stream)
     torch.cuda.synchronize()
     res_ms = r0.elapsed_time(r1)
-    n_mism = int(mism.item())
+    del graph_r
+    diff = (YR[args.warmup:] != Y[args.warmup:]).reshape(args.steps * L, -1).any(dim=1)
+    n_mism = int(diff.sum().item())
     # pinned host -> device copy rate for blob-sized copies (the fills' own size)
     blob = st.blob_bytes
     dst = torch.empty((64, blob), dtype=torch.uint8, device="cuda")
@@ -520,12 +547,15 @@ def run_stack(args, shape):
                                         f"pinned backing store limited to {L} layers by host memory"),
                    "l2": f"pool {L * shape.pool_slots * st.stride / 1e9:.1f} GB and {L} resident layers, "
                          "far beyond L2", "build_s": t_build},
-        "pool": {"hit_rate": d["hits"] / lookups, "misses_per_token": d["misses"] / K,
+        "pool": {"policy": "LFU + recency, run on the device (lookup and fill kernels); timed tokens are one "
+                           "CUDA graph", "hit_rate": d["hits"] / lookups, "misses_per_token": d["misses"] / K,
                  "fill_bytes_per_token": d["bytes_filled"] / K, "evictions": d["evictions"],
-                 "exposed_copy_us_per_token": d["exposed_copy_ns"] / 1e3 / K,
+                 "added_us_per_token": (ms - res_ms) * 1e3 / K,
+                 "fill_gbs_effective": d["bytes_filled"] / max((ms - res_ms) * 1e-3, 1e-9) / 1e9,
                  "pcie_h2d_gbs_blob_copies": h2d_gbs,
                  "copy_bound_us_per_token": d["bytes_filled"] / K / (h2d_gbs * 1e9) * 1e6},
-        "resident": {"tokens_per_s": K / (res_ms * 1e-3), "note": "same tokens, all experts resident, eager calls"},
+        "resident": {"tokens_per_s": K / (res_ms * 1e-3),
+                     "note": "same tokens, all experts resident, one CUDA graph"},
         "bit_identical_to_resident": n_mism == 0, "mismatched_layer_outputs": n_mism,
         "all_outputs_finite": bool(torch.isfinite(Y[args.warmup:].float()).all()),
         "layer_outputs_compared": K * L,
@@ -555,6 +585,116 @@ def routing_trace(shape, layer: int, tokens: int):
     if r["router_bias"] is not None:
         logits = logits + r["router_bias"]
     return torch.topk(logits, shape.top_k, dim=1).indices.to(torch.int32)
+
+
+def run_pool_sweep(args, shape):
+    """Tokens/s of a stack of 80B-shaped layers served from the bounded pool
+    (device-side LFU + recency, timed tokens as one CUDA graph) against the
+    pool size (1/8, 1/4, 1/2 of each layer's experts) and the skew of the
+    routing (router bias Zipf s = 0.6, 1.1, 1.6), with the all-resident stack
+    on the same tokens beside each point."""
+    from int4_routed_expert_06_b300 import binding as B
+    from int4_routed_expert_06_b300 import build as _build
+    from int4_routed_expert_06_b300.stack import PooledStack
+    _build.build()
+    torch.cuda.set_device(0)
+    E = shape.n_experts
+    L = min(8, max(1, int(0.4 * host_bytes_available()) // (E * synth.expert_bytes(shape))))
+    base = [synth.make_layer(shape, seed=shape.weight_seed + l, device="cuda") for l in range(L)]
+    zipfs, fracs = (0.6, 1.1, 1.6), (8, 4, 2)
+    W, K = max(16, args.warmup), max(8, args.steps)
+    x0 = synth.decode_xs(shape, W + K, seed0=synth.STACK_X_SEED0, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def run_graph(fwd):
+        with torch.cuda.stream(stream):
+            for j in range(W):
+                fwd(j)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(W, W + K):
+                fwd(j)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return K / (e0.elapsed_time(e1) * 1e-3)
+
+    y = torch.empty((1, shape.hidden), dtype=torch.bfloat16, device="cuda")
+    table = []
+    with ClockSampler(0) as clk:
+        for zs in zipfs:
+            sz = dataclasses.replace(shape, zipf_s=zs)
+            ws_ = []
+            for l in range(L):
+                w = dict(base[l])
+                w["router_bias"] = synth.zipf_router_bias(sz, shape.weight_seed + l, device="cuda")
+                ws_.append(w)
+            resident = [B.DeviceLayer(sz, ws_[l], torch.arange(E, dtype=torch.int32)) for l in range(L)]
+            cfg = resident[0].cfg
+            nb = B.moe_layer_workspace_bytes(cfg, 1)
+            wsb = torch.empty(nb, dtype=torch.uint8, device="cuda")
+
+            def fwd_res(j):
+                h = x0[j:j + 1]
+                for l in range(L):
+                    B.moe_layer_forward(cfg, resident[l].struct(), layer_input(h), 1, y, None, None, None, wsb, nb,
+                                        stream)
+                    h = (h.float() + y.float()).to(torch.bfloat16)
+
+            res_tps = run_graph(fwd_res)
+            del resident
+            for fr in fracs:
+                st = PooledStack(sz, L, E // fr, lambda l: ws_[l], device_policy=True)
+                st.workspace(1)
+
+                def fwd_pool(j):
+                    h = x0[j:j + 1]
+                    for l in range(L):
+                        st.layer_forward(l, layer_input(h), y, stream=stream)
+                        h = (h.float() + y.float()).to(torch.bfloat16)
+
+                s_0 = None
+                with torch.cuda.stream(stream):
+                    for j in range(W):
+                        fwd_pool(j)
+                torch.cuda.synchronize()
+                s_0 = st.stats()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for j in range(W, W + K):
+                        fwd_pool(j)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    e0.record(stream)
+                    g.replay()
+                    e1.record(stream)
+                torch.cuda.synchronize()
+                tps = K / (e0.elapsed_time(e1) * 1e-3)
+                s_1 = st.stats()
+                if B.moe_get_device_error() != 0:
+                    raise RuntimeError("a kernel recorded a device error during the pool sweep")
+                hits, misses = s_1["hits"] - s_0["hits"], s_1["misses"] - s_0["misses"]
+                table.append({"zipf_s": zs, "pool_fraction": 1.0 / fr, "slots_per_layer": E // fr,
+                              "tokens_per_s": round(tps, 1), "hit_rate": round(hits / max(hits + misses, 1), 4),
+                              "misses_per_token": round(misses / K, 2),
+                              "resident_tokens_per_s": round(res_tps, 1)})
+                del g
+                st.close()
+    head = next(r for r in table if r["zipf_s"] == 1.1 and r["pool_fraction"] == 0.25)
+    print(json.dumps({
+        "metric": f"{L}-layer 80B-stack decode tokens/s through the bounded pool against pool size and routing skew",
+        "value": head["tokens_per_s"], "unit": "tokens/s", "n_gpus": 1, "steps": K, "warmup": W,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "s32/f32", "data": "synthetic",
+        "config": {"workload": f"{L} layers x E={E} top-{shape.top_k} int4, batch-1 decode, pool 1/8, 1/4, 1/2 of "
+                               "each layer's experts, router bias Zipf s = 0.6, 1.1, 1.6, LFU + recency on the device",
+                   "value_at": "pool 1/4, Zipf s = 1.1",
+                   "timing": "warm-up tokens eager, then the timed tokens (every layer) as one CUDA graph"},
+        "sweep": table, "clocks": clk.summary(), "gpu_launches": None,
+    }), flush=True)
 
 
 def run_batch_sweep(args, shape):
@@ -696,7 +836,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="80b-dec",
                     choices=["80b-dec", "35b-dec", "80b-dec-int8", "35b-dec-int8", "80b-prefill", "80b-stack",
-                             "80b-batch", "policy-study"])
+                             "80b-batch", "80b-pool-sweep", "policy-study"])
     ap.add_argument("--tokens", type=int, default=1000, help="decode tokens per bench step")
     ap.add_argument("--replicas", type=int, default=0, help="layer copies to rotate through (0 = >= 3x L2)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -714,6 +854,10 @@ def main():
     if args.workload == "80b-batch":
         if rank == 0:
             run_batch_sweep(args, synth.DEC_80B)
+        return
+    if args.workload == "80b-pool-sweep":
+        if rank == 0:
+            run_pool_sweep(args, synth.STACK_80B)
         return
     shape = synth.SHAPES[args.workload]
 
