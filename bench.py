@@ -26,7 +26,10 @@ at batch 1); no collective touches the data path.
 `--workload 35b-dec`, `80b-dec-int8` and `35b-dec-int8` time the same decode
 loop on the 35B-shaped layer and on both layers with affine int8 codes.
 
-Four more workloads print their own line (not the default):
+Five more workloads print their own line (not the default):
+
+- `--workload 80b-stack-file`: the stack with the expert backing store on a
+  file (one pread per missed expert, then one copy into its slot).
 
 - `--workload 80b-pool-sweep`: tokens/s and hit rate of an 8-layer stack
   through the bounded pool (device-side policy) against pool size and
@@ -587,6 +590,93 @@ def routing_trace(shape, layer: int, tokens: int):
     return torch.topk(logits, shape.top_k, dim=1).indices.to(torch.int32)
 
 
+def fs_type(path: str) -> str:
+    """File-system type of the mount holding path (from /proc/mounts)."""
+    best, typ = "", "unknown"
+    try:
+        real = os.path.realpath(path)
+        with open("/proc/mounts") as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) >= 3 and real.startswith(parts[1]) and len(parts[1]) > len(best):
+                    best, typ = parts[1], parts[2]
+    except OSError:
+        pass
+    return typ
+
+
+def run_stack_file(args, shape):
+    """The stack served from the bounded pool with the backing store on a
+    file (the storage tier below host memory): one pread per missed expert
+    into pinned staging, then one copy into its slot; host-side policy,
+    eager per-layer calls.  Layers limited by the free space of --tier-dir."""
+    import shutil
+    import tempfile
+    from int4_routed_expert_06_b300 import binding as B
+    from int4_routed_expert_06_b300 import build as _build
+    from int4_routed_expert_06_b300.stack import PooledStack
+    _build.build()
+    torch.cuda.set_device(0)
+    tdir = args.tier_dir or tempfile.gettempdir()
+    E = shape.n_experts
+    per_layer = E * ((synth.expert_bytes(shape) + 4095) // 4096 * 4096)
+    L = max(1, min(8, int(0.5 * shutil.disk_usage(tdir).free) // per_layer))
+    path = os.path.join(tdir, f"moe_stack_{os.getpid()}.qpack")
+    try:
+        t_build = time.perf_counter()
+        st = PooledStack(shape, L, shape.pool_slots,
+                         lambda l: synth.make_layer(shape, seed=shape.weight_seed + l, device="cuda"),
+                         file_path=path, readers=args.readers)
+        t_build = time.perf_counter() - t_build
+        n = args.warmup + args.steps
+        x0 = synth.decode_xs(shape, n, seed0=synth.STACK_X_SEED0, device="cuda")
+        y = torch.empty((1, shape.hidden), dtype=torch.bfloat16, device="cuda")
+
+        def token(j):
+            h = x0[j:j + 1]
+            for l in range(L):
+                st.layer_forward(l, layer_input(h), y)
+                h = (h.float() + y.float()).to(torch.bfloat16)
+
+        for j in range(args.warmup):
+            token(j)
+        torch.cuda.synchronize()
+        s0, f0 = st.stats(), B.slot_pool_file_stats(st.handle)
+        t0 = time.perf_counter()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for j in range(args.warmup, n):
+            token(j)
+        e1.record()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        ms = e0.elapsed_time(e1)
+        s1, f1 = st.stats(), B.slot_pool_file_stats(st.handle)
+        if B.moe_get_device_error() != 0:
+            raise RuntimeError("a kernel recorded a device error during the bench")
+        K = args.steps
+        hits, misses = s1["hits"] - s0["hits"], s1["misses"] - s0["misses"]
+        rb, rns = f1["bytes_read"] - f0["bytes_read"], f1["read_ns"] - f0["read_ns"]
+        print(json.dumps({
+            "metric": f"{L}-layer 80B-stack decode tokens/s with the expert backing store on a file",
+            "value": K / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": K, "warmup": args.warmup,
+            "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "s32/f32", "data": "synthetic",
+            "config": {"workload": f"{L} layers x E={E} top-{shape.top_k} int4, {shape.pool_slots} slots/layer, "
+                                   f"Zipf(s={shape.zipf_s}) router bias, batch-1 decode, backing store on a file",
+                       "file_system": fs_type(tdir), "direct_io": f1["direct"], "readers": args.readers,
+                       "file_gb": L * per_layer / 1e9, "build_s": t_build},
+            "tier": {"hit_rate": hits / max(hits + misses, 1), "misses_per_token": misses / K,
+                     "read_gbs": rb / max(rns * 1e-9, 1e-9) / 1e9, "read_ms_per_token": rns / 1e6 / K,
+                     "bytes_read_per_token": rb / K},
+            "wall_s": wall,
+        }), flush=True)
+        st.close()
+    finally:
+        if os.path.exists(path):
+            os.remove(path)
+
+
 def run_pool_sweep(args, shape):
     """Tokens/s of a stack of 80B-shaped layers served from the bounded pool
     (device-side LFU + recency, timed tokens as one CUDA graph) against the
@@ -836,7 +926,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="80b-dec",
                     choices=["80b-dec", "35b-dec", "80b-dec-int8", "35b-dec-int8", "80b-prefill", "80b-stack",
-                             "80b-batch", "80b-pool-sweep", "policy-study"])
+                             "80b-batch", "80b-pool-sweep", "80b-stack-file", "policy-study"])
+    ap.add_argument("--tier-dir", default="", help="directory of the stack-file workload's backing file")
+    ap.add_argument("--readers", type=int, default=4, help="read threads of the file tier")
     ap.add_argument("--tokens", type=int, default=1000, help="decode tokens per bench step")
     ap.add_argument("--replicas", type=int, default=0, help="layer copies to rotate through (0 = >= 3x L2)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -858,6 +950,10 @@ def main():
     if args.workload == "80b-pool-sweep":
         if rank == 0:
             run_pool_sweep(args, synth.STACK_80B)
+        return
+    if args.workload == "80b-stack-file":
+        if rank == 0:
+            run_stack_file(args, synth.STACK_80B)
         return
     shape = synth.SHAPES[args.workload]
 

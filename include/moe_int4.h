@@ -306,6 +306,26 @@ moe_status moe_pooled_layer_forward(const moe_config *cfg, slot_pool *p, int32_t
                                     float *y_f32, int32_t *topk_idx_out, void *workspace,
                                     size_t ws_bytes, cudaStream_t stream);
 
+/* Storage tier below host memory: a pool whose backing store is a file of
+ * fixed-stride blobs, expert e of layer l at file_offset + (l * E + e) *
+ * file_stride (file_stride and file_offset multiples of 4096, file_stride at
+ * least the blob rounded up to 4096), as written by the caller (the blob
+ * bytes of moe_pack_expert, zero padded).  The file is opened read-only with
+ * O_DIRECT where the file system allows it (else buffered).  A fill reads
+ * each missing blob with pread, `readers` (1..64) host threads at a time,
+ * into one of 16 pinned staging buffers whose previous copy has finished,
+ * then copies it to its slot on side_stream: one read and one copy per
+ * expert.  The device slots are the blob size rounded up to 256 bytes apart
+ * (pool_bytes >= n_layers * slots_per_layer * that).  The policy runs on the
+ * host (slot_pool_enable_device is refused).  slot_pool_file_stats: bytes
+ * read, nanoseconds spent in the reads, and whether they bypass the page
+ * cache (direct = 1). */
+moe_status slot_pool_create_file(const moe_config *cfg, int32_t n_layers, int32_t slots_per_layer,
+                                 void *pool_dev, size_t pool_bytes, const char *path, size_t file_offset,
+                                 size_t file_stride, int32_t readers, cudaStream_t side_stream,
+                                 slot_pool **out);
+moe_status slot_pool_file_stats(slot_pool *p, int64_t *bytes_read, int64_t *read_ns, int32_t *direct);
+
 /* Device-side policy.  slot_pool_enable_device switches a pool that has
  * served no host lookup to running its rule on the device: the same rule,
  * the same tie breaks and the same clock as slot_pool_lookup, kept in device

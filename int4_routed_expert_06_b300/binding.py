@@ -101,6 +101,8 @@ _SIGS = {
     "slot_pool_destroy": (None, [_P]),
     "slot_pool_set_policy": (_I, [_P, _I]),
     "slot_pool_enable_device": (_I, [_P]),
+    "slot_pool_create_file": (_I, [_CP(moe_config), _I, _I, _P, _Z, C.c_char_p, _Z, _Z, _I, _P, _CP(_P)]),
+    "slot_pool_file_stats": (_I, [_P, _CP(C.c_int64), _CP(C.c_int64), _CP(_I)]),
     "slot_pool_step_device": (_I, [_P, _I, _P, _I, _P]),
     "moe_get_device_error": (_I, [_P]),
     "moe_last_error_message": (C.c_char_p, []),
@@ -287,6 +289,22 @@ MOE_POOL_LFU_RECENCY, MOE_POOL_LRU, MOE_POOL_LFU = 0, 1, 2
 
 def slot_pool_set_policy(pool: int, policy: int) -> None:
     _check(lib().slot_pool_set_policy(pool, policy), "slot_pool_set_policy")
+
+
+def slot_pool_create_file(cfg, n_layers, slots_per_layer, pool_dev, pool_bytes, path: str, file_offset: int,
+                          file_stride: int, readers: int = 4, side_stream=None) -> int:
+    out = C.c_void_p()
+    _check(lib().slot_pool_create_file(C.byref(cfg), n_layers, slots_per_layer, _ptr(pool_dev), pool_bytes,
+                                       path.encode(), file_offset, file_stride, readers,
+                                       _stream(side_stream) if side_stream is not None else None, C.byref(out)),
+           "slot_pool_create_file")
+    return out.value
+
+
+def slot_pool_file_stats(pool: int) -> dict:
+    b, ns, d = C.c_int64(0), C.c_int64(0), C.c_int32(0)
+    _check(lib().slot_pool_file_stats(pool, C.byref(b), C.byref(ns), C.byref(d)), "slot_pool_file_stats")
+    return {"bytes_read": b.value, "read_ns": ns.value, "direct": bool(d.value)}
 
 
 def slot_pool_enable_device(pool: int) -> None:

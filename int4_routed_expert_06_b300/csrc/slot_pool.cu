@@ -12,7 +12,15 @@
 //           slot starts at use count 1.
 // Two comparison rules are selectable for studies (slot_pool_set_policy):
 // LRU, the smallest (stamp, slot id), and LFU, the smallest (use count, slot id).
+#include <fcntl.h>
+#include <sys/stat.h>
+#include <unistd.h>
+
+#include <algorithm>
+#include <chrono>
 #include <mutex>
+#include <string>
+#include <thread>
 #include <vector>
 
 #include "internal.h"
@@ -244,6 +252,15 @@ struct slot_pool {
     long long *d_freq = nullptr, *d_stamp = nullptr; // [L*S]
     long long *d_ctr = nullptr;            // clock, lookups, hits, misses, evictions, bytes_filled
     int32_t *d_fills = nullptr;            // [L][1 + 2*S]: count, then (expert, slot) pairs of the last lookup
+    // storage tier (slot_pool_create_file): blobs read from a file of
+    // fixed-stride records into pinned staging buffers, then copied to slots
+    int fd = -1;
+    bool direct = false;                   // opened with O_DIRECT
+    size_t file_stride = 0, file_off0 = 0;
+    int n_readers = 0;
+    std::vector<char *> staging;           // pinned, file_stride bytes each
+    std::vector<cudaEvent_t> staging_ev;   // the copy out of each buffer
+    int64_t read_ns = 0, bytes_read = 0;
 };
 
 extern "C" moe_status slot_pool_create(const moe_config *cfg, int32_t n_layers, int32_t slots_per_layer,
@@ -312,6 +329,159 @@ static moe_status ensure_table_dev(slot_pool *p)
         return cuda_check(e, "slot pool device table");
     }
     p->table_dev = t;
+    return MOE_OK;
+}
+
+// ------------------------------------------------------------ storage tier
+
+constexpr int kStaging = 16;   // pinned staging buffers (one blob each)
+constexpr size_t kIoAlign = 4096;
+
+static size_t up_io(size_t v) { return (v + kIoAlign - 1) / kIoAlign * kIoAlign; }
+
+// Read `bytes` at `off` of the pool's file into dst, whole: pread until done.
+static bool read_full(int fd, char *dst, size_t bytes, off_t off)
+{
+    size_t got = 0;
+    while (got < bytes) {
+        const ssize_t r = pread(fd, dst + got, bytes - got, off + (off_t)got);
+        if (r <= 0)
+            return false;
+        got += (size_t)r;
+    }
+    return true;
+}
+
+// The fills of one lookup from the file: in batches of kStaging, each blob
+// read (by n_readers threads) into a staging buffer whose previous copy has
+// finished, then copied to its slot on the side stream.  Called with p->mu held.
+static moe_status file_fill(slot_pool *p, int32_t layer, const std::vector<Fill> &fills)
+{
+    using namespace moe;
+    if (p->staging.empty()) {
+        for (int i = 0; i < kStaging; ++i) {
+            char *b = nullptr;
+            cudaEvent_t ev = nullptr;
+            cudaError_t e = cudaHostAlloc(reinterpret_cast<void **>(&b), p->file_stride, cudaHostAllocDefault);
+            if (e == cudaSuccess)
+                e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+            if (e != cudaSuccess) {
+                if (b)
+                    cudaFreeHost(b);
+                return cuda_check(e, "slot_pool_fill: staging buffers");
+            }
+            p->staging.push_back(b);
+            p->staging_ev.push_back(ev);
+        }
+    }
+    const size_t rb = p->direct ? up_io(p->blob_bytes) : p->blob_bytes; // bytes one read takes
+    const int E = p->s.E;
+    for (size_t b0 = 0; b0 < fills.size(); b0 += kStaging) {
+        const int nb = (int)std::min(fills.size() - b0, (size_t)kStaging);
+        for (int i = 0; i < nb; ++i) { // the buffer's last copy must have finished
+            cudaError_t e = cudaEventSynchronize(p->staging_ev[i]);
+            if (e != cudaSuccess)
+                return cuda_check(e, "slot_pool_fill: staging reuse");
+        }
+        const auto t0 = std::chrono::steady_clock::now();
+        std::vector<char> ok(nb, 0);
+        auto work = [&](int w) {
+            for (int i = w; i < nb; i += p->n_readers) {
+                const Fill &f = fills[b0 + i];
+                const off_t off = (off_t)(p->file_off0 + ((size_t)layer * E + f.expert) * p->file_stride);
+                ok[i] = read_full(p->fd, p->staging[i], rb, off) ? 1 : 0;
+            }
+        };
+        std::vector<std::thread> th;
+        for (int w = 1; w < std::min(p->n_readers, nb); ++w)
+            th.emplace_back(work, w);
+        work(0);
+        for (auto &t : th)
+            t.join();
+        p->read_ns += (int64_t)std::chrono::duration_cast<std::chrono::nanoseconds>(
+                          std::chrono::steady_clock::now() - t0)
+                          .count();
+        for (int i = 0; i < nb; ++i) {
+            if (!ok[i])
+                return fail(MOE_ERR_CUDA, "slot_pool_fill: read of expert %d of layer %d from the file failed",
+                            fills[b0 + i].expert, layer);
+            char *dst = p->pool + ((size_t)layer * p->S + fills[b0 + i].slot) * p->stride;
+            cudaError_t e = cudaMemcpyAsync(dst, p->staging[i], p->blob_bytes, cudaMemcpyHostToDevice, p->side);
+            if (e == cudaSuccess)
+                e = cudaEventRecord(p->staging_ev[i], p->side);
+            if (e != cudaSuccess)
+                return cuda_check(e, "slot_pool_fill: copy");
+            p->st.bytes_filled += (int64_t)p->blob_bytes;
+            p->bytes_read += (int64_t)rb;
+        }
+    }
+    return MOE_OK;
+}
+
+extern "C" moe_status slot_pool_create_file(const moe_config *cfg, int32_t n_layers, int32_t slots_per_layer,
+                                            void *pool_dev, size_t pool_bytes, const char *path, size_t file_offset,
+                                            size_t file_stride, int32_t readers, cudaStream_t side_stream,
+                                            slot_pool **out)
+{
+    using namespace moe;
+    if (!out || !path)
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_create_file: NULL argument");
+    *out = nullptr;
+    if (readers < 1 || readers > 64)
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_create_file: readers %d outside [1, 64]", readers);
+    if (file_stride % kIoAlign || file_offset % kIoAlign)
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_create_file: file_stride and file_offset must be multiples of %zu",
+                    kIoAlign);
+    moe_blob_layout lay;
+    moe_status ls = moe_blob_layout_get(cfg, cfg ? cfg->inter : 0, &lay);
+    if (ls != MOE_OK)
+        return ls;
+    if (file_stride < up_io(lay.bytes))
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_create_file: file_stride %zu < %zu (blob rounded to 4 KiB)",
+                    file_stride, up_io(lay.bytes));
+    bool direct = true;
+    int fd = open(path, O_RDONLY | O_DIRECT);
+    if (fd < 0) { // a file system without direct I/O: buffered reads
+        direct = false;
+        fd = open(path, O_RDONLY);
+    }
+    if (fd < 0)
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_create_file: cannot open %s", path);
+    struct stat sbuf;
+    const size_t need = file_offset + (size_t)n_layers * (size_t)(cfg->n_experts > 0 ? cfg->n_experts : 0) * file_stride;
+    if (fstat(fd, &sbuf) != 0 || (size_t)sbuf.st_size < need) {
+        close(fd);
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_create_file: %s holds fewer than the %zu bytes of %d layers",
+                    path, need, n_layers);
+    }
+    // the pool itself, with a placeholder backing address (never read in this mode)
+    moe_status st = slot_pool_create(cfg, n_layers, slots_per_layer, pool_dev, pool_bytes, pool_dev,
+                                     lay.bytes <= 256 ? 256 : (lay.bytes + 255) / 256 * 256, side_stream, out);
+    if (st != MOE_OK) {
+        close(fd);
+        return st;
+    }
+    slot_pool *p = *out;
+    p->backing = nullptr;
+    p->fd = fd;
+    p->direct = direct;
+    p->file_stride = file_stride;
+    p->file_off0 = file_offset;
+    p->n_readers = readers;
+    return MOE_OK;
+}
+
+extern "C" moe_status slot_pool_file_stats(slot_pool *p, int64_t *bytes_read, int64_t *read_ns, int32_t *direct)
+{
+    using namespace moe;
+    if (!p || !bytes_read || !read_ns || !direct)
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_file_stats: NULL argument");
+    std::lock_guard<std::mutex> g(p->mu);
+    if (p->fd < 0)
+        return fail(MOE_ERR_INVALID_ARG, "slot_pool_file_stats: the pool has no file tier");
+    *bytes_read = p->bytes_read;
+    *read_ns = p->read_ns;
+    *direct = p->direct ? 1 : 0;
     return MOE_OK;
 }
 
@@ -438,13 +608,19 @@ extern "C" moe_status slot_pool_fill(slot_pool *p, int32_t layer, const int32_t 
     if (ts != MOE_OK)
         return ts;
     const int E = p->s.E;
-    for (const Fill &f : fills) {
-        char *dst = p->pool + ((size_t)layer * p->S + f.slot) * p->stride;
-        const char *src = p->backing + ((size_t)layer * E + f.expert) * p->stride;
-        cudaError_t e = cudaMemcpyAsync(dst, src, p->blob_bytes, cudaMemcpyHostToDevice, p->side);
-        if (e != cudaSuccess)
-            return cuda_check(e, "slot_pool_fill: copy");
-        p->st.bytes_filled += (int64_t)p->blob_bytes;
+    if (p->fd >= 0) {
+        moe_status fs = file_fill(p, layer, fills);
+        if (fs != MOE_OK)
+            return fs;
+    } else {
+        for (const Fill &f : fills) {
+            char *dst = p->pool + ((size_t)layer * p->S + f.slot) * p->stride;
+            const char *src = p->backing + ((size_t)layer * E + f.expert) * p->stride;
+            cudaError_t e = cudaMemcpyAsync(dst, src, p->blob_bytes, cudaMemcpyHostToDevice, p->side);
+            if (e != cudaSuccess)
+                return cuda_check(e, "slot_pool_fill: copy");
+            p->st.bytes_filled += (int64_t)p->blob_bytes;
+        }
     }
     for (size_t j0 = 0; j0 < fills.size(); j0 += kMaxUpdates) {
         TableUpdate u{};
@@ -654,6 +830,8 @@ extern "C" moe_status slot_pool_enable_device(slot_pool *p)
     if (p->S > kMaxUniq * 2)
         return fail(MOE_ERR_UNSUPPORTED, "slot_pool_enable_device: %d slots per layer (at most %d)", p->S,
                     kMaxUniq * 2);
+    if (p->fd >= 0)
+        return fail(MOE_ERR_UNSUPPORTED, "slot_pool_enable_device: a file-backed pool fills from the host");
     cudaPointerAttributes at{};
     if (cudaPointerGetAttributes(&at, p->backing) != cudaSuccess || at.type != cudaMemoryTypeHost ||
         !at.devicePointer) {
@@ -739,6 +917,13 @@ extern "C" void slot_pool_destroy(slot_pool *p)
             cudaFree(d);
     if (p->pinned_ids)
         cudaFreeHost(p->pinned_ids);
+    for (size_t i = 0; i < p->staging.size(); ++i) {
+        cudaEventSynchronize(p->staging_ev[i]);
+        cudaEventDestroy(p->staging_ev[i]);
+        cudaFreeHost(p->staging[i]);
+    }
+    if (p->fd >= 0)
+        close(p->fd);
     if (p->fill_done)
         cudaEventDestroy(p->fill_done);
     if (p->wait_begin)

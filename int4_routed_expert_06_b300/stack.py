@@ -10,7 +10,8 @@ the caller's stream, with the fills read from the pinned backing store.
 """
 from __future__ import annotations
 
-from typing import Callable, Dict, List
+import os
+from typing import Callable, Dict, List, Optional
 
 import torch
 
@@ -20,20 +21,29 @@ from . import binding as B
 class PooledStack:
     def __init__(self, shape, n_layers: int, slots_per_layer: int,
                  layer_weights: Callable[[int], Dict[str, torch.Tensor]], device: str = "cuda",
-                 device_policy: bool = False):
+                 device_policy: bool = False, file_path: Optional[str] = None, readers: int = 4):
         self.shape, self.cfg = shape, B.config_for(shape)
         self.L, self.S, self.E = n_layers, slots_per_layer, shape.n_experts
         lay = B.moe_blob_layout_get(self.cfg, shape.inter)
         self.blob_bytes = lay.bytes
         self.stride = (lay.bytes + 255) // 256 * 256
-        self.backing = torch.empty((n_layers, self.E, self.stride), dtype=torch.uint8, pin_memory=True)
+        # backing store: pinned host memory, or (file_path) a file of 4 KiB-aligned records
+        self.file_path = file_path
+        self.file_stride = (lay.bytes + 4095) // 4096 * 4096
+        self.backing = None if file_path else torch.empty((n_layers, self.E, self.stride), dtype=torch.uint8,
+                                                           pin_memory=True)
+        fh = open(file_path, "wb") if file_path else None
         self.pool = torch.empty((n_layers * slots_per_layer * self.stride,), dtype=torch.uint8, device=device)
         ident = torch.arange(self.E, dtype=torch.int32)
         self.resident: List[dict] = []
         for l in range(n_layers):
             w = layer_weights(l)
-            blobs = B.pack_blobs(self.cfg, shape.inter, w, ident, self.E, self.stride)
-            self.backing[l].copy_(blobs)
+            if fh is not None:
+                blobs = B.pack_blobs(self.cfg, shape.inter, w, ident, self.E, self.file_stride)
+                fh.write(blobs.cpu().numpy().tobytes())
+            else:
+                blobs = B.pack_blobs(self.cfg, shape.inter, w, ident, self.E, self.stride)
+                self.backing[l].copy_(blobs)
             del blobs
             sh_lay = B.moe_blob_layout_get(self.cfg, shape.shared_inter)
             sh_stride = (sh_lay.bytes + 255) // 256 * 256
@@ -46,8 +56,16 @@ class PooledStack:
                 r["w_shared_gate"].data_ptr(), shared.data_ptr())
             self.resident.append(r)
         self.side = torch.cuda.Stream()
-        self.handle = B.slot_pool_create(self.cfg, n_layers, slots_per_layer, self.pool, self.pool.numel(),
-                                         self.backing, self.stride, self.side)
+        if fh is not None:
+            fh.flush()
+            os.fsync(fh.fileno())
+            os.posix_fadvise(fh.fileno(), 0, 0, os.POSIX_FADV_DONTNEED)  # reads come from the device, not RAM
+            fh.close()
+            self.handle = B.slot_pool_create_file(self.cfg, n_layers, slots_per_layer, self.pool, self.pool.numel(),
+                                                  file_path, 0, self.file_stride, readers, self.side)
+        else:
+            self.handle = B.slot_pool_create(self.cfg, n_layers, slots_per_layer, self.pool, self.pool.numel(),
+                                             self.backing, self.stride, self.side)
         self.device_policy = device_policy
         if device_policy:  # lookup and fills as kernels on the caller's stream: no host round trip
             B.slot_pool_enable_device(self.handle)
@@ -71,6 +89,14 @@ class PooledStack:
         """Copy of layer l's device table row ([E] int32)."""
         ptr, _ = B.slot_pool_layer(self.handle, l)
         return torch.as_tensor(_DeviceArray(ptr, self.E), device=self.pool.device).clone()
+
+    def blob(self, l: int, e: int) -> torch.Tensor:
+        """Expert e of layer l as the backing store holds it (CPU bytes)."""
+        if self.backing is not None:
+            return self.backing[l, e, :self.blob_bytes]
+        with open(self.file_path, "rb") as f:
+            f.seek((l * self.E + e) * self.file_stride)
+            return torch.frombuffer(bytearray(f.read(self.blob_bytes)), dtype=torch.uint8)
 
     def slot_bytes(self, l: int, slot: int) -> torch.Tensor:
         base = (l * self.S + slot) * self.stride

@@ -186,3 +186,29 @@ def test_kernel_path_values_and_workspace_follow_the_path():
         assert B.moe_layer_workspace_bytes(cfg, 1) == one      # T = 1 stays on the single-token kernels
     finally:
         B.moe_set_kernel_path(0)
+
+
+def test_file_tier_pool_validates_on_the_host(tmp_path):
+    """slot_pool_create_file checks path, alignment and file size before any
+    device work; a valid one is created and destroyed without a GPU."""
+    cfg = B.config_for(synth.DEC_80B)
+    lay = B.moe_blob_layout_get(cfg, synth.DEC_80B.inter)
+    fstride = (lay.bytes + 4095) // 4096 * 4096
+    E = synth.DEC_80B.n_experts
+    path = tmp_path / "one_layer.qpack"
+    with open(path, "wb") as f:
+        f.truncate(E * fstride)
+    fake_pool = 1 << 20                                   # never dereferenced on the host
+    with pytest.raises(B.MoEError) as ei:
+        B.slot_pool_create_file(cfg, 1, 8, fake_pool, 8 * fstride, str(tmp_path / "missing"), 0, fstride)
+    assert ei.value.status == B.MOE_ERR_INVALID_ARG
+    with pytest.raises(B.MoEError):
+        B.slot_pool_create_file(cfg, 1, 8, fake_pool, 8 * fstride, str(path), 0, fstride - 256)   # not 4 KiB
+    with pytest.raises(B.MoEError):
+        B.slot_pool_create_file(cfg, 2, 8, fake_pool, 16 * fstride, str(path), 0, fstride)      # file too small
+    h = B.slot_pool_create_file(cfg, 1, 8, fake_pool, 8 * fstride, str(path), 0, fstride, readers=2)
+    try:
+        st = B.slot_pool_file_stats(h)
+        assert st["bytes_read"] == 0 and st["read_ns"] == 0
+    finally:
+        B.slot_pool_destroy(h)

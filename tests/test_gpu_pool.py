@@ -33,10 +33,11 @@ def weights():
     return [synth.make_layer(SHAPE, seed=40 + l, device="cuda") for l in range(SHAPE.layers)]
 
 
-@pytest.fixture(scope="module", params=["host", "device"])
-def stack(request, weights):
+@pytest.fixture(scope="module", params=["host", "device", "file"])
+def stack(request, weights, tmp_path_factory):
+    path = str(tmp_path_factory.mktemp("tier") / "layers.qpack") if request.param == "file" else None
     st = PooledStack(SHAPE, SHAPE.layers, SHAPE.pool_slots, lambda l: weights[l],
-                     device_policy=request.param == "device")
+                     device_policy=request.param == "device", file_path=path)
     resident = [B.DeviceLayer(SHAPE, weights[l], torch.arange(SHAPE.n_experts, dtype=torch.int32))
                 for l in range(SHAPE.layers)]
     yield st, weights, resident
@@ -44,7 +45,8 @@ def stack(request, weights):
 
 
 def test_pool_stack_bit_identical_to_resident_and_policy_exact(stack):
-    """Host and device policy: the same outputs, tables and counters."""
+    """Host policy, device policy, and host policy over the file tier: the
+    same outputs, tables and counters."""
     st, weights, resident = stack
     L, E, k = SHAPE.layers, SHAPE.n_experts, SHAPE.top_k
     policy = SlotPolicy(L, E, SHAPE.pool_slots)
@@ -73,7 +75,7 @@ def test_pool_stack_bit_identical_to_resident_and_policy_exact(stack):
             assert host == policy.table[l], (step, l)
             assert st.table_device(l).tolist() == host
             for e, s in fills:                      # freshly filled slots hold the backing blob
-                assert torch.equal(st.slot_bytes(l, s).cpu(), st.backing[l, e, :st.blob_bytes])
+                assert torch.equal(st.slot_bytes(l, s).cpu(), st.blob(l, e))
             if step % 8 == 3:                        # oracle on the GPU's own layer input
                 ref = oracles[l].forward(x)
                 if not near_tie_tokens(ref["logits"], k)[0]:
@@ -87,6 +89,9 @@ def test_pool_stack_bit_identical_to_resident_and_policy_exact(stack):
     assert s["bytes_filled"] == policy.misses * st.blob_bytes
     assert s["lookups"] == 24 * L
     assert (s["exposed_copy_ns"] > 0) == (not st.device_policy)
+    if st.file_path:
+        f = B.slot_pool_file_stats(st.handle)
+        assert f["bytes_read"] >= policy.misses * st.blob_bytes and f["read_ns"] > 0
     assert policy.hits > 0 and policy.evictions > 0
 
 
