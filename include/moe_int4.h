@@ -4,11 +4,14 @@
  * The layer is the sparse MoE block of the Qwen3-Next / Qwen3.5-3.6 hybrid
  * models that the Swiftlet project pages describe: each token is routed to
  * top_k of n_experts SwiGLU experts (10 of 512 for the 80B model, 8 of 256
- * for 35B; page 2 "How it works"), a shared expert stays resident beside the
+ * for 35B; the Swiftlet README "How it works"), a shared expert stays resident beside the
  * router (same section), weights use MLX affine 4-bit group quantisation
- * (page 2 "Relation to TurboFieldfare"), routed experts are packed as
+ * (Swiftlet README "Relation to TurboFieldfare"), routed experts are packed as
  * fixed-stride blobs so that one expert is one copy, and a bounded pool
- * caches hot experts with LFU-plus-recency eviction (page 2 "How it works").
+ * caches hot experts with LFU-plus-recency eviction (Swiftlet README "How it works").
+ * "Swiftlet README" is the project README as reposted under the title
+ * "Swiftlet：在 Mac 上运行 80B 版 Qwen（内存 4.3 GB），在 iPhone 上运行 35B 版";
+ * section names are given in English.
  *
  * Conventions for every call:
  *   - Pointers named *_dev / device are CUDA device pointers; *_host are host
@@ -58,7 +61,7 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_F16 = 2 } moe_dtype;
  *   router_dtype: router and shared-gate weights, MOE_F32 or MOE_BF16.
  *   qscale_dtype: per-group scale and bias, MOE_F32 or MOE_F16.
  *   bits: code width of the expert weights, 4 or 8 (MLX affine int4 or
- *   int8 group quantisation, page 2 "Relation to TurboFieldfare"); 0 means
+ *   int8 group quantisation, the Swiftlet README "Relation to TurboFieldfare"); 0 means
  *   4, so a zero-initialised field keeps the int4 layout. */
 typedef struct {
     int32_t hidden;
@@ -117,7 +120,7 @@ size_t moe_bucket_workspace_bytes(const moe_config *cfg, int32_t T);
 size_t moe_expert_workspace_bytes(const moe_config *cfg, int32_t T);
 size_t moe_layer_workspace_bytes(const moe_config *cfg, int32_t T);
 
-/* Router and top-k (pages: page 2 "How it works", k of E experts per token;
+/* Router and top-k (pages: the Swiftlet README "How it works", k of E experts per token;
  * the renormalised softmax follows the Qwen MoE layer).
  *   x [T, H] act_dtype; w_router [E, H] router_dtype; router_bias [E] fp32 or
  *   NULL; w_shared_gate [H] router_dtype or NULL (required iff I_s > 0).
@@ -134,8 +137,11 @@ moe_status moe_route(const moe_config *cfg, const void *x, int32_t T, const void
                      float *topk_w, float *shared_gate_logit, float *logits_out,
                      void *workspace, size_t ws_bytes, cudaStream_t stream);
 
-/* Token -> expert bucketing: a stable counting sort of the T*k (token, rank)
- * pairs of topk_idx [T, k] by expert.  counts [E], offsets [E+1] (exclusive
+/* Token -> expert bucketing (Swiftlet README "Correctness": sparse MoE routing, each
+ * token's k experts; the pages give no bucketing step, this is how the
+ * many-token path groups a routed batch by expert for its grouped GEMMs):
+ * a stable counting sort of the T*k (token, rank) pairs of topk_idx [T, k]
+ * by expert.  counts [E], offsets [E+1] (exclusive
  * prefix sum), perm_tok [T*k] and perm_rank [T*k] list the pairs in
  * (expert, token, rank) order.  Device pointers.  Ids outside [0, E) are
  * recorded as MOE_ERR_DEVICE_FAULT and dropped. */
@@ -143,8 +149,11 @@ moe_status moe_bucket(const moe_config *cfg, const int32_t *topk_idx, int32_t T,
                       int32_t *offsets, int32_t *perm_tok, int32_t *perm_rank, void *workspace,
                       size_t ws_bytes, cudaStream_t stream);
 
-/* One expert on T tokens, no routing weight: y[t] = W_d (silu(W_g x[t]) *
- * (W_u x[t])) with intermediate `inter`.  e holds device pointers.  y [T, H]
+/* One expert on T tokens, no routing weight (Swiftlet README "How it works": each
+ * expert a SwiGLU MLP, gate and up from H to inter, down back to H, weights
+ * in MLX affine int4/int8 group quantisation, the Swiftlet README "Relation to
+ * TurboFieldfare"): y[t] = W_d (silu(W_g x[t]) * (W_u x[t])) with
+ * intermediate `inter`.  e holds device pointers.  y [T, H]
  * act_dtype; y_f32 [T, H] fp32 or NULL (the value before rounding). */
 moe_status moe_expert_forward(const moe_config *cfg, const moe_expert *e, int32_t inter,
                               const void *x, int32_t T, void *y, float *y_f32, void *workspace,

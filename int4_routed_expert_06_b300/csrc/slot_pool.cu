@@ -2,7 +2,7 @@
 //
 // The Swiftlet pages keep hot routed experts in a bounded pool of slots,
 // fetch a missing expert with one read of its fixed-stride blob, and evict by
-// "LFU plus recency" (page 2 "How it works" and "Relation to
+// "LFU plus recency" (Swiftlet README "How it works" and "Relation to
 // TurboFieldfare").  Here the pool lives in HBM, the backing store is pinned
 // host memory, a fill is one cudaMemcpyAsync per expert on a side stream, and
 // the policy runs on the host:

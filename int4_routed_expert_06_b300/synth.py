@@ -20,7 +20,7 @@ implement):
   * scale and bias are row-major [out, in // G] in the scale dtype.
 
 Shapes follow the workloads the project pages describe (Qwen3-Next-80B-A3B:
-10 of 512 experts; Qwen3.6-35B-A3B: 8 of 256 experts, page 2 "How it works"),
+10 of 512 experts; Qwen3.6-35B-A3B: 8 of 256 experts, the Swiftlet README "How it works"),
 with hidden 2048, expert intermediate 512 and group 64.
 """
 from __future__ import annotations
@@ -70,7 +70,7 @@ STACK_80B = MoEShape("80b-stack", 2048, 512, 10, 512, 512, 64, "bf16", "bf16", "
 PREFILL_80B = MoEShape("80b-prefill", 2048, 512, 10, 512, 512, 64, "bf16", "bf16",
                        "f16", 0.02, 0.02, tokens=4096, zipf_s=1.1, weight_seed=2)
 
-# The same layers with affine int8 codes (page 2 "Relation to TurboFieldfare"
+# The same layers with affine int8 codes (Swiftlet README "Relation to TurboFieldfare"
 # names int4 and int8 group quantisation).
 DEC_35B_INT8 = dataclasses.replace(DEC_35B, name="35b-dec-int8", bits=8)
 DEC_80B_INT8 = dataclasses.replace(DEC_80B, name="80b-dec-int8", bits=8)

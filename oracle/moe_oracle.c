@@ -11,12 +11,12 @@
  *
  * What it follows (Swiftlet project pages):
  *   - each layer routes each token to 10 of 512 (80B) or 8 of 256 (35B)
- *     experts (page 2 "How it works");
- *   - the router and a shared expert are resident (page 2 "How it works");
+ *     experts (Swiftlet README "How it works");
+ *   - the router and a shared expert are resident (Swiftlet README "How it works");
  *   - weights use MLX affine int4 or int8 group quantisation,
- *     W ~= scale*q + bias per group (page 2 "Relation to TurboFieldfare");
+ *     W ~= scale*q + bias per group (Swiftlet README "Relation to TurboFieldfare");
  *   - the layer is checked against an exact CPU reference, and streaming an
- *     expert from cache or from storage never changes the result (page 2
+ *     expert from cache or from storage never changes the result (Swiftlet README
  *     "Correctness").
  * The softmax over the selected experts, the SwiGLU expert MLP and the
  * sigmoid gate of the shared expert follow the Qwen3-Next / Qwen3.5-3.6

@@ -9,7 +9,7 @@ imports nothing from here.
 Conversions to double (bf16, fp16 and fp32 to float64) are exact, so every
 input reaches the C code bit-for-bit.
 
-Layer (Swiftlet project pages, page 2 "How it works": k of E routed experts
+Layer (Swiftlet project pages, the Swiftlet README "How it works": k of E routed experts
 plus a resident shared expert; the combine, SwiGLU and sigmoid gate follow the
 Qwen3-Next / Qwen3.5-3.6 layer the pages name):
     logits = W_r x + b,  s = w_sg . x

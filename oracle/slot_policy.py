@@ -1,6 +1,6 @@
 """Slot-pool policy oracle: LFU + recency eviction (TEST INFRASTRUCTURE ONLY).
 
-The Swiftlet pages (page 2 "How it works" and "Relation to TurboFieldfare")
+The Swiftlet pages (Swiftlet README "How it works" and "Relation to TurboFieldfare")
 cache hot routed experts in a bounded pool of slots and evict by "LFU plus
 recency"; they do not spell the rule out.  The reading written here:
 

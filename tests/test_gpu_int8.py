@@ -3,7 +3,7 @@ scales and biases as int4) on the 35B- and 80B-shaped layers: the
 single-token kernels and the generic ones at T = 1 against the oracle, a
 ragged batch on the generic kernels, and one routed expert alone.
 
-Page 2, "Relation to TurboFieldfare": MLX affine int4/int8 group
+The Swiftlet README, "Relation to TurboFieldfare": MLX affine int4/int8 group
 quantisation.
 """
 import numpy as np

@@ -3,7 +3,7 @@ sends them through the tcgen05 grouped GEMMs (token columns padded to 16)
 instead of the generic kernels.  Every token is checked against the oracle
 on the 80B-shaped layer, and against the generic kernels.
 
-Page 2, "Four ways to use it": the OpenAI-compatible server batches the
+The Swiftlet README, "Four ways to use it": the OpenAI-compatible server batches the
 tokens of concurrent sequences into one layer call.
 """
 import numpy as np
