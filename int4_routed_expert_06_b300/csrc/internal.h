@@ -108,7 +108,7 @@ struct Layout {
 Layout layout(const Shape &s, int T);
 // The shape and token count take the grouped GEMMs under the calling
 // thread's kernel path: bf16 activations, 4-bit codes, H a multiple of 128,
-// I and I_s multiples of 64, a shared expert, T >= min_tokens().
+// I and I_s multiples of 128, a shared expert, T >= min_tokens().
 bool wanted(const Shape &s, int T);
 // wanted() on a Blackwell (sm_10x) device with the tensor-map encoder.
 bool eligible(const Shape &s, int T);

@@ -14,7 +14,7 @@
 // The GEMMs run "swap-AB": the M = 128 side of each MMA is a tile of weight
 // rows, dequantised from int4 by four warps straight into the 128-byte
 // swizzled K-major shared-memory layout the MMA reads; the N side is the
-// expert's tokens (rounded up to 16, at most 256 per unit), brought in by TMA
+// expert's tokens (rounded up to 16, at most 128 per unit), brought in by TMA
 // with the matching swizzle.  Skewed routing then costs at most 15 padded
 // token columns per unit instead of a 128-row tile.  The shared expert is one
 // more group, over all T tokens.
@@ -26,21 +26,26 @@
 namespace moe {
 namespace prefill {
 
-constexpr int kNch = 256;        // tokens per unit (MMA N <= 256)
-constexpr int kBK = 64;          // K per pipeline stage (one 128-byte swizzle atom of bf16)
-constexpr int kStages = 3;       // A (dequantised) and B (token) tiles
+constexpr int kNch = 128;        // tokens per unit (MMA N <= 256)
+constexpr int kAtomK = 64;       // K of one 128-byte swizzle atom of bf16
+constexpr int kBK = 128;         // K per pipeline stage: two atoms, so that the per-stage
+                                 // synchronisation is paid once per 128 K
+constexpr int kSub = kBK / kAtomK;
+constexpr int kStages = 2;       // A (dequantised) and B (token) tiles
 constexpr int kCStages = 3;      // staged code tiles (run ahead of the dequant)
 constexpr int kCK = 256;         // K of one code stage: 128-byte row pieces (whole lines)
 constexpr int kBoxRows = 32;     // TMA box: 32 rows x 64 bf16
 // warps 0-15 dequant, 16 weight TMA, 17 token TMA, 18 MMA, 19-22 epilogue
 constexpr int kDqWarps = 16, kCodeWarp = 16, kRowWarp = 17, kMmaWarp = 18;
 constexpr int kThreads = 32 * 23;
-constexpr uint32_t kATile = 128 * 128;         // 16 KB
-constexpr uint32_t kBTile = kNch * 128;        // 32 KB
+constexpr uint32_t kATile = 128 * kBK * 2;     // 32 KB: kSub atoms of [128 rows][128 B]
+constexpr uint32_t kBTile = kNch * kBK * 2;    // 32 KB: kSub atoms of [kNch rows][128 B]
 constexpr uint32_t kCTile = 128 * (kCK / 2);   // 16 KB: 128 rows x 256 codes
 constexpr uint32_t kSTile = 16 * 1024;         // a unit's scale and bias rows (at most 4 x 64 rows x 64 B)
 constexpr uint32_t kPTile = 16 * 1024;         // the same as (scale, bias) pairs [group][128 rows] (<= 32 groups)
 constexpr uint32_t kSmem = kStages * (kATile + kBTile) + kCStages * kCTile + kSTile + kPTile + 1024;
+static_assert(kCK % kBK == 0, "a code stage holds whole pipeline stages");
+static_assert(kSmem <= 232448, "dynamic shared memory of one CTA");
 constexpr uint64_t kWaitNs = 500ull * 1000 * 1000; // 0.5 s bound on any single wait
 
 struct Unit {
@@ -348,7 +353,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ volatile int s_abort;
     __shared__ volatile int s_dq_fail; // set only: a dequant wait gave up (read only after dq_sync)
 
-    unsigned char *smem = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    // 1024-byte aligned tiles, as an offset from the shared array, so that the
+    // compiler keeps every access in the shared window (no generic accesses)
+    const uint32_t raw_base = smem_u32(smem_raw);
+    unsigned char *smem = smem_raw + (((raw_base + 1023u) & ~1023u) - raw_base);
     unsigned char *a_tiles = smem;
     unsigned char *b_tiles = a_tiles + kStages * kATile;
     unsigned char *c_ring = b_tiles + kStages * kBTile;
@@ -454,14 +462,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         wfail = true;
                         break;
                     }
-                    unsigned char *row = a_tiles + as * kATile + r * 128;
-                    if (ok) {
-                        const uint2 qw = *reinterpret_cast<const uint2 *>(cp + (k0 - kc) / 2 + q * 8);
-                        const SBPair<TS> p = s_pair[((k0 + 16 * q) / G) * 128 + r];
-                        dequant_quarter(qw, to_f32(p.s), to_f32(p.b), row, r, q);
-                    } else {
-                        *reinterpret_cast<uint4 *>(row + (2 * q) * 16) = make_uint4(0, 0, 0, 0);
-                        *reinterpret_cast<uint4 *>(row + (2 * q + 1) * 16) = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                    for (int j = 0; j < kSub; ++j) { // atom j: K columns k0 + 64 j ..
+                        unsigned char *row = a_tiles + as * kATile + j * (128 * 128) + r * 128;
+                        if (ok) {
+                            const uint2 qw =
+                                *reinterpret_cast<const uint2 *>(cp + (k0 - kc) / 2 + j * (kAtomK / 2) + q * 8);
+                            const SBPair<TS> p = s_pair[((k0 + kAtomK * j + 16 * q) / G) * 128 + r];
+                            dequant_quarter(qw, to_f32(p.s), to_f32(p.b), row, r, q);
+                        } else {
+                            *reinterpret_cast<uint4 *>(row + (2 * q) * 16) = make_uint4(0, 0, 0, 0);
+                            *reinterpret_cast<uint4 *>(row + (2 * q + 1) * 16) = make_uint4(0, 0, 0, 0);
+                        }
                     }
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     __syncwarp();
@@ -563,10 +575,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         s_abort = 1;
                         break;
                     }
-                    bar_expect(&b_full[stage], (uint32_t)nbox * kBoxRows * 128);
+                    bar_expect(&b_full[stage], (uint32_t)(nbox * kSub) * kBoxRows * 128);
                     unsigned char *tile = b_tiles + stage * kBTile;
-                    for (int bx = 0; bx < nbox; ++bx)
-                        tma_load_2d(tile + bx * kBoxRows * 128, map, k0, row0 + bx * kBoxRows, &b_full[stage]);
+                    for (int j = 0; j < kSub; ++j)
+                        for (int bx = 0; bx < nbox; ++bx)
+                            tma_load_2d(tile + j * (kNch * 128) + bx * kBoxRows * 128, map, k0 + j * kAtomK,
+                                        row0 + bx * kBoxRows, &b_full[stage]);
                     if (++stage == kStages) {
                         stage = 0;
                         ph ^= 1;
@@ -601,9 +615,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t a_addr = smem_u32(a_tiles + stage * kATile);
                     const uint32_t b_addr = smem_u32(b_tiles + stage * kBTile);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        mma_bf16(d_tmem, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32), idesc,
+                    for (int kk = 0; kk < kBK / 16; ++kk) { // atom kk / 4, 16-column step kk % 4 within it
+                        const uint32_t ao = (uint32_t)(kk / 4) * (128 * 128) + (uint32_t)(kk % 4) * 32;
+                        const uint32_t bo = (uint32_t)(kk / 4) * (kNch * 128) + (uint32_t)(kk % 4) * 32;
+                        mma_bf16(d_tmem, sw128_desc(a_addr + ao), sw128_desc(b_addr + bo), idesc,
                                  (k0 > 0 || kk > 0) ? 1u : 0u);
+                    }
                     mma_commit(&ab_empty[stage]);
                     if (++stage == kStages) {
                         stage = 0;
@@ -708,7 +725,7 @@ static bool make_map(CUtensorMap *m, const void *base, long rows, int cols)
         return false;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBoxRows};
+    cuuint32_t box[2] = {(cuuint32_t)kAtomK, (cuuint32_t)kBoxRows};
     cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -807,7 +824,7 @@ bool wanted(const Shape &s, int T)
 {
     if (kernel_path() == 1 || T < min_tokens() || T > 65536)
         return false;
-    return s.act == MOE_BF16 && s.bits == 4 && s.H % 128 == 0 && s.I % 64 == 0 && s.Is % 64 == 0 && s.Is > 0;
+    return s.act == MOE_BF16 && s.bits == 4 && s.H % 128 == 0 && s.I % kBK == 0 && s.Is % kBK == 0 && s.Is > 0;
 }
 
 bool eligible(const Shape &s, int T)
