@@ -208,6 +208,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
     __shared__ int s_cnt[1024];
     __shared__ int s_ord[1024];
     __shared__ int s_scan[1024];
+    __shared__ int s_slot[1024]; // by rank position: the expert's slot
     const int e = threadIdx.x;
     s_cnt[e] = e < E ? counts[e] : -1;
     __syncthreads();
@@ -235,28 +236,43 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
         s_scan[e] += v;
         __syncthreads();
     }
-    const int sh_units = has_shared ? n_ft_sh * ((T + kNch - 1) / kNch) : 0;
-    if (e == 0 && has_shared) {
-        int u = 0;
-        for (int c0 = 0; c0 < T; c0 += kNch)
-            for (int ft = 0; ft < n_ft_sh; ++ft)
-                units[u++] = {-1, ft, c0, min(kNch, T - c0), 0};
+    if (e < E) {
+        const int sl = table[ex];
+        s_slot[e] = sl >= 0 && sl < n_slots ? sl : -1;
     }
-    if (e < E && nu > 0) {
-        int u = sh_units + s_scan[e] - nu;
-        const int base = offsets[ex], cnt = s_cnt[ex];
-        const int sl = table[ex], slot = sl >= 0 && sl < n_slots ? sl : -1;
-        for (int c0 = 0; c0 < cnt; c0 += kNch)
-            for (int ft = 0; ft < n_ft; ++ft)
-                units[u++] = {ex, ft, base + c0, min(kNch, cnt - c0), slot};
+    __syncthreads();
+    // every unit written by the CTA together: unit u -> (expert at rank p,
+    // token chunk, feature tile), chunk major within an expert
+    const int n_ch_sh = has_shared ? (T + kNch - 1) / kNch : 0;
+    const int sh_units = n_ft_sh * n_ch_sh;
+    const int total = sh_units + s_scan[1023];
+    for (int u = e; u < total; u += blockDim.x) {
+        if (u < sh_units) {
+            const int c = u / n_ft_sh, ft = u - c * n_ft_sh;
+            units[u] = {-1, ft, c * kNch, min(kNch, T - c * kNch), 0};
+        } else {
+            const int v = u - sh_units;
+            int lo = 0, hi = E - 1; // first rank position p with s_scan[p] > v
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (s_scan[mid] > v)
+                    hi = mid;
+                else
+                    lo = mid + 1;
+            }
+            const int p = lo, ex2 = s_ord[p], first = s_scan[p] - n_ft * ((s_cnt[ex2] + kNch - 1) / kNch);
+            const int local = v - first, c = local / n_ft, ft = local - c * n_ft;
+            units[u] = {ex2, ft, offsets[ex2] + c * kNch, min(kNch, s_cnt[ex2] - c * kNch), s_slot[p]};
+        }
     }
     if (e == 1023)
-        *n_units = sh_units + s_scan[1023];
+        *n_units = total;
 }
 
-// y[t, h] = sum_r P[inv[t, r], h] + P[T*k + t, h]; bf16 y and optional fp32.
-__global__ void combine_kernel(const float *__restrict__ P, const int32_t *__restrict__ inv, int T, int k, int H,
-                               int has_shared, __nv_bfloat16 *__restrict__ y, float *__restrict__ y32)
+// y[t, h] = sum_r P[inv[t, r], h] + P[T*k + t, h]; bf16 y and optional fp32,
+// one output a thread (any alignment of y and y32).
+__global__ void combine_scalar_kernel(const float *__restrict__ P, const int32_t *__restrict__ inv, int T, int k,
+                                      int H, int has_shared, __nv_bfloat16 *__restrict__ y, float *__restrict__ y32)
 {
     const long n = (long)T * H;
     for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
@@ -269,6 +285,40 @@ __global__ void combine_kernel(const float *__restrict__ P, const int32_t *__res
         y[i] = __float2bfloat16_rn(acc);
         if (y32)
             y32[i] = acc;
+    }
+}
+
+// The same sum in the same order, four consecutive h a thread (16-byte loads;
+// H a multiple of 4, y 8-byte and y32 16-byte aligned).
+__global__ void combine_kernel(const float *__restrict__ P, const int32_t *__restrict__ inv, int T, int k, int H,
+                               int has_shared, __nv_bfloat16 *__restrict__ y, float *__restrict__ y32)
+{
+    const int H4 = H >> 2;
+    const long n = (long)T * H4;
+    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+        const int t = (int)(i / H4), h4 = (int)(i - (long)t * H4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int r = 0; r < k; ++r) {
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(P + (long)inv[t * k + r] * H) + h4);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        if (has_shared) {
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(P + ((long)T * k + t) * H) + h4);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 packed;
+        packed.x = *reinterpret_cast<uint32_t *>(&lo);
+        packed.y = *reinterpret_cast<uint32_t *>(&hi);
+        reinterpret_cast<uint2 *>(y + (long)t * H)[h4] = packed;
+        if (y32)
+            reinterpret_cast<float4 *>(y32 + (long)t * H)[h4] = acc;
     }
 }
 
@@ -930,7 +980,12 @@ cudaError_t experts_forward(const Shape &s, const ExpertSrc &src, const void *x,
                               : gemm_go<float>(m_act, m_act, w_dn, g, st);
     if (e != cudaSuccess)
         return e;
-    combine_kernel<<<4 * sm_count(), 256, 0, st>>>(pout, inv, T, s.k, s.H, 1, static_cast<__nv_bfloat16 *>(y), y32);
+    if ((reinterpret_cast<uintptr_t>(y) & 7) == 0 && (reinterpret_cast<uintptr_t>(y32) & 15) == 0)
+        combine_kernel<<<4 * sm_count(), 256, 0, st>>>(pout, inv, T, s.k, s.H, 1, static_cast<__nv_bfloat16 *>(y),
+                                                        y32);
+    else
+        combine_scalar_kernel<<<4 * sm_count(), 256, 0, st>>>(pout, inv, T, s.k, s.H, 1,
+                                                               static_cast<__nv_bfloat16 *>(y), y32);
     return cudaGetLastError();
 }
 
