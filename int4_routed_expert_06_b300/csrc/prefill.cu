@@ -31,19 +31,22 @@ constexpr int kAtomK = 64;       // K of one 128-byte swizzle atom of bf16
 constexpr int kBK = 128;         // K per pipeline stage: two atoms, so that the per-stage
                                  // synchronisation is paid once per 128 K
 constexpr int kSub = kBK / kAtomK;
-constexpr int kStages = 2;       // A (dequantised) and B (token) tiles
+constexpr int kStages = 4;       // A (dequantised, in TMEM) and B (token, in shared memory) stages
 constexpr int kCStages = 3;      // staged code tiles (run ahead of the dequant)
 constexpr int kCK = 256;         // K of one code stage: 128-byte row pieces (whole lines)
 constexpr int kBoxRows = 32;     // TMA box: 32 rows x 64 bf16
 // warps 0-15 dequant, 16 weight TMA, 17 token TMA, 18 MMA, 19-22 epilogue
 constexpr int kDqWarps = 16, kCodeWarp = 16, kRowWarp = 17, kMmaWarp = 18;
 constexpr int kThreads = 32 * 23;
-constexpr uint32_t kATile = 128 * kBK * 2;     // 32 KB: kSub atoms of [128 rows][128 B]
+constexpr uint32_t kACols = kBK / 2;           // TMEM columns of one A stage: 128 rows x kBK bf16
+constexpr uint32_t kAccCols = kNch;            // TMEM columns of one fp32 accumulator
+constexpr uint32_t kACol0 = 2 * kAccCols;      // the A stages follow the two accumulators
+static_assert(kACol0 + kStages * kACols <= 512, "TMEM columns of one CTA");
 constexpr uint32_t kBTile = kNch * kBK * 2;    // 32 KB: kSub atoms of [kNch rows][128 B]
 constexpr uint32_t kCTile = 128 * (kCK / 2);   // 16 KB: 128 rows x 256 codes
 constexpr uint32_t kSTile = 16 * 1024;         // a unit's scale and bias rows (at most 4 x 64 rows x 64 B)
 constexpr uint32_t kPTile = 16 * 1024;         // the same as (scale, bias) pairs [group][128 rows] (<= 32 groups)
-constexpr uint32_t kSmem = kStages * (kATile + kBTile) + kCStages * kCTile + kSTile + kPTile + 1024;
+constexpr uint32_t kSmem = kStages * kBTile + kCStages * kCTile + kSTile + kPTile + 1024;
 static_assert(kCK % kBK == 0, "a code stage holds whole pipeline stages");
 static_assert(kSmem <= 232448, "dynamic shared memory of one CTA");
 constexpr uint64_t kWaitNs = 500ull * 1000 * 1000; // 0.5 s bound on any single wait
@@ -137,15 +140,6 @@ __host__ __device__ __forceinline__ uint32_t idesc_bf16(int M, int N)
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate)
-{
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-                 : "memory");
-}
-
 __device__ __forceinline__ void mma_commit(uint64_t *bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -160,6 +154,28 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
                    "=r"(r[15])
                  : "r"(taddr));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Store 16 columns of this warp's 32 TMEM lanes (one row a thread).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+                 "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// D (TMEM) += A (TMEM: 128 lanes = rows, two bf16 of K a column) . B (shared
+// memory descriptor).
+__device__ __forceinline__ void mma_bf16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+                 "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+                 : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -347,20 +363,18 @@ struct WMaps {
     CUtensorMap shared[6];
 };
 
-// One stage of one tile row quarter: 16 codes (two code words, columns
-// k0 + 16q .. + 15, one quantisation group) -> 16 bf16 w = s q + b (fp32
-// arithmetic, one rounding), written as 16-byte chunks 2q, 2q + 1 of row r
-// of the swizzled K-major tile (chunk c at position c ^ (r & 7)).
-__device__ __forceinline__ void dequant_quarter(uint2 qw, float s, float b, unsigned char *row, int r, int q)
+// 32 codes of one weight row (four code words, one quantisation group) ->
+// 32 bf16 w = s q + b (fp32 arithmetic, one rounding), packed two a word in K
+// order: out[j] holds columns 2j, 2j + 1.
+__device__ __forceinline__ void dequant_32(uint4 qw, float s, float b, uint32_t (&out)[16])
 {
-    const uint32_t w[2] = {qw.x, qw.y};
+    const uint32_t w[4] = {qw.x, qw.y, qw.z, qw.w};
     const float s16 = 16.f * s, b16 = b - s16;
 #pragma unroll
-    for (int cc = 0; cc < 2; ++cc) { // 16-byte chunk = 8 columns = one code word
+    for (int cc = 0; cc < 4; ++cc) { // one code word = 8 columns
         const uint32_t word = w[cc];
         const uint32_t lo = ((word << 3) & 0x78787878u) | 0x80808080u;
         const uint32_t hi = ((word >> 1) & 0x78787878u) | 0x80808080u;
-        uint32_t packed[4];
 #pragma unroll
         for (int bb = 0; bb < 4; ++bb) {
             const uint32_t sel = 0x7044u | (uint32_t)(bb << 8);
@@ -368,10 +382,8 @@ __device__ __forceinline__ void dequant_quarter(uint2 qw, float s, float b, unsi
             const float f1 = __uint_as_float(__byte_perm(hi, 0x3F000000u, sel)); // column 2bb + 1
             const float2 wv = __ffma2_rn(make_float2(f0, f1), make_float2(s16, s16), make_float2(b16, b16));
             __nv_bfloat162 h2 = __floats2bfloat162_rn(wv.x, wv.y);
-            packed[bb] = *reinterpret_cast<uint32_t *>(&h2);
+            out[4 * cc + bb] = *reinterpret_cast<uint32_t *>(&h2);
         }
-        const int c = 2 * q + cc;
-        *reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4)) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
     }
 }
 
@@ -407,8 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // compiler keeps every access in the shared window (no generic accesses)
     const uint32_t raw_base = smem_u32(smem_raw);
     unsigned char *smem = smem_raw + (((raw_base + 1023u) & ~1023u) - raw_base);
-    unsigned char *a_tiles = smem;
-    unsigned char *b_tiles = a_tiles + kStages * kATile;
+    unsigned char *b_tiles = smem;
     unsigned char *c_ring = b_tiles + kStages * kBTile;
     unsigned char *s_raw = c_ring + kCStages * kCTile;
     SBPair<TS> *s_pair = reinterpret_cast<SBPair<TS> *>(s_raw + kSTile); // [group][128 rows]
@@ -452,11 +463,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto next_unit = [&](int ui, const Unit &cur) { return ui + grid < nu ? A.units[ui + grid] : cur; };
 
     if (warp < kDqWarps) {
-        // ---------------- dequant: thread t takes tile row t / 4, K quarter t % 4.
-        // The named barrier dq_sync joins exactly these warps, so they leave the
-        // unit loop together: a failed wait sets s_dq_fail, and the decision
-        // to stop is read after the next dq_sync.
-        const int t = threadIdx.x, r = t >> 2, q = t & 3;
+        // ---------------- dequant: warp w writes TMEM lanes 32 (w % 4) .. + 31
+        // (one weight row a thread), K part w / 4 (32 K) of each stage, with
+        // tcgen05.st into the stage's A columns.  The named barrier dq_sync
+        // joins exactly these warps, so they leave the unit loop together: a
+        // failed wait sets s_dq_fail, and the decision to stop is read after
+        // the next dq_sync.
+        const int t = threadIdx.x, qd = warp & 3, part = warp >> 2, r = qd * 32 + lane;
+        const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16) + kACol0 + (uint32_t)part * (kACols / 4);
         int cs = 0, as = 0;
         uint32_t cph = 0, aph = 0, sph = 0;
         Unit u = blockIdx.x < nu ? A.units[blockIdx.x] : Unit{};
@@ -494,8 +508,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             dq_sync(); // the pairs are complete and the raw rows free
             if (t == 0)
                 bar_arrive(&s_empty);
-            // this row's code piece (kCK / 2 bytes) in a code stage
-            const int coff = A.mode == 0 ? (r & 1) * (64 * kCK / 2) + (r >> 1) * (kCK / 2) : r * (kCK / 2);
+            // this row's code piece (kCK / 2 bytes, 16-byte chunks 128-byte
+            // swizzled by the copy) in a code stage
+            const int brow = A.mode == 0 ? (r >> 1) : r; // row within its box
+            const int coff = (A.mode == 0 ? (r & 1) * (kCTile / 2) : 0) + brow * (kCK / 2);
             bool wfail = false; // warp-uniform
             for (int kc = 0; kc < K && !wfail; kc += kCK) {
                 if (!__all_sync(0xFFFFFFFFu, bar_wait(&c_full[cs], cph))) {
@@ -512,20 +528,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         wfail = true;
                         break;
                     }
+                    uint32_t packed[16];
+                    if (ok) {
+                        const int c16 = ((k0 - kc) >> 5) + part; // 16-byte chunk of the row piece
+                        const uint4 qw = *reinterpret_cast<const uint4 *>(cp + ((c16 ^ (brow & 7)) << 4));
+                        const SBPair<TS> p = s_pair[((k0 + 32 * part) / G) * 128 + r];
+                        dequant_32(qw, to_f32(p.s), to_f32(p.b), packed);
+                    } else {
 #pragma unroll
-                    for (int j = 0; j < kSub; ++j) { // atom j: K columns k0 + 64 j ..
-                        unsigned char *row = a_tiles + as * kATile + j * (128 * 128) + r * 128;
-                        if (ok) {
-                            const uint2 qw =
-                                *reinterpret_cast<const uint2 *>(cp + (k0 - kc) / 2 + j * (kAtomK / 2) + q * 8);
-                            const SBPair<TS> p = s_pair[((k0 + kAtomK * j + 16 * q) / G) * 128 + r];
-                            dequant_quarter(qw, to_f32(p.s), to_f32(p.b), row, r, q);
-                        } else {
-                            *reinterpret_cast<uint4 *>(row + (2 * q) * 16) = make_uint4(0, 0, 0, 0);
-                            *reinterpret_cast<uint4 *>(row + (2 * q + 1) * 16) = make_uint4(0, 0, 0, 0);
-                        }
+                        for (int j = 0; j < 16; ++j)
+                            packed[j] = 0u;
                     }
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    tmem_st16(trow + (uint32_t)as * kACols, packed);
+                    tmem_st_wait();
+                    tc_fence_before();
                     __syncwarp();
                     if (lane == 0)
                         bar_arrive(&a_full[as]);
@@ -650,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int K = kdim(u);
                 const int N = (u.n + 15) & ~15;
                 const uint32_t idesc = idesc_bf16(128, N);
-                const uint32_t d_tmem = tmem + (uint32_t)(acc * 256);
+                const uint32_t d_tmem = tmem + (uint32_t)acc * kAccCols;
                 if (!bar_wait(&acc_empty[acc], acc_ph ^ 1)) {
                     s_abort = 1;
                     break;
@@ -662,14 +678,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(a_tiles + stage * kATile);
+                    const uint32_t a_t = tmem + kACol0 + (uint32_t)stage * kACols;
                     const uint32_t b_addr = smem_u32(b_tiles + stage * kBTile);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) { // atom kk / 4, 16-column step kk % 4 within it
-                        const uint32_t ao = (uint32_t)(kk / 4) * (128 * 128) + (uint32_t)(kk % 4) * 32;
+                    for (int kk = 0; kk < kBK / 16; ++kk) { // B atom kk / 4, 16-column step kk % 4 within it
                         const uint32_t bo = (uint32_t)(kk / 4) * (kNch * 128) + (uint32_t)(kk % 4) * 32;
-                        mma_bf16(d_tmem, sw128_desc(a_addr + ao), sw128_desc(b_addr + bo), idesc,
-                                 (k0 > 0 || kk > 0) ? 1u : 0u);
+                        mma_bf16_ta(d_tmem, a_t + (uint32_t)kk * 8, sw128_desc(b_addr + bo), idesc,
+                                    (k0 > 0 || kk > 0) ? 1u : 0u);
                     }
                     mma_commit(&ab_empty[stage]);
                     if (++stage == kStages) {
@@ -701,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            const uint32_t t_row = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * 256);
+            const uint32_t t_row = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)acc * kAccCols;
             const int rowb = (u.e < 0) ? A.T * A.k + u.j0 : u.j0; // first output row of the unit
             for (int c0 = 0; c0 < u.n; c0 += 16) {
                 uint32_t v[16];
@@ -785,7 +800,8 @@ static bool make_map(CUtensorMap *m, const void *base, long rows, int cols)
 // 3-D map over one weight array of every slot of a pool: elements of a
 // row (inner), rows, slots; no swizzle.
 static bool make_wmap(CUtensorMap *m, CUtensorMapDataType dt, size_t esz, const char *base, uint64_t inner,
-                      uint64_t rows, uint64_t slots, uint64_t slot_stride, uint32_t box_inner, uint32_t box_rows)
+                      uint64_t rows, uint64_t slots, uint64_t slot_stride, uint32_t box_inner, uint32_t box_rows,
+                      CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
@@ -794,9 +810,8 @@ static bool make_wmap(CUtensorMap *m, CUtensorMapDataType dt, size_t esz, const 
     cuuint64_t strides[2] = {inner * esz, slot_stride};
     cuuint32_t box[3] = {box_inner, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, dt, 3, const_cast<char *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
+    return fn(m, dt, 3, const_cast<char *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // The weight-side maps of one GEMM kind (mode 0 gate/up, 1 down), for the
@@ -814,15 +829,15 @@ static bool make_wmaps(const Shape &s, const ExpertSrc &src, int mode, WMaps *w)
         bool ok;
         if (mode == 0) {
             ok = make_wmap(&m[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base + off[M_QG], s.H / 2, inter, slots, stride,
-                           kCK / 2, 64) &&
+                           kCK / 2, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
                  make_wmap(&m[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base + off[M_QU], s.H / 2, inter, slots, stride,
-                           kCK / 2, 64);
+                           kCK / 2, 64, CU_TENSOR_MAP_SWIZZLE_128B);
             const size_t so[4] = {off[M_SG], off[M_BG], off[M_SU], off[M_BU]};
             for (int j = 0; ok && j < 4; ++j)
                 ok = make_wmap(&m[2 + j], sdt, sb, base + so[j], s.H / s.G, inter, slots, stride, s.H / s.G, 64);
         } else {
             ok = make_wmap(&m[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base + off[M_QD], inter / 2, s.H, slots, stride,
-                           kCK / 2, 128) &&
+                           kCK / 2, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
                  make_wmap(&m[1], sdt, sb, base + off[M_SD], inter / s.G, s.H, slots, stride, inter / s.G, 128) &&
                  make_wmap(&m[2], sdt, sb, base + off[M_BD], inter / s.G, s.H, slots, stride, inter / s.G, 128);
         }
