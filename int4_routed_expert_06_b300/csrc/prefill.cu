@@ -14,7 +14,7 @@
 // The GEMMs run "swap-AB": the M = 128 side of each MMA is a tile of weight
 // rows, dequantised from int4 by four warps straight into the 128-byte
 // swizzled K-major shared-memory layout the MMA reads; the N side is the
-// expert's tokens (rounded up to 16, at most 128 per unit), brought in by TMA
+// expert's tokens (rounded up to 16, at most 192 per unit), brought in by TMA
 // with the matching swizzle.  Skewed routing then costs at most 15 padded
 // token columns per unit instead of a 128-row tile.  The shared expert is one
 // more group, over all T tokens.
@@ -26,12 +26,12 @@
 namespace moe {
 namespace prefill {
 
-constexpr int kNch = 128;        // tokens per unit (MMA N <= 256)
+constexpr int kNch = 192;        // tokens per unit (MMA N <= 256)
 constexpr int kAtomK = 64;       // K of one 128-byte swizzle atom of bf16
 constexpr int kBK = 128;         // K per pipeline stage: two atoms, so that the per-stage
                                  // synchronisation is paid once per 128 K
 constexpr int kSub = kBK / kAtomK;
-constexpr int kStages = 4;       // A (dequantised, in TMEM) and B (token, in shared memory) stages
+constexpr int kStages = 2;       // A (dequantised, in TMEM) and B (token, in shared memory) stages
 constexpr int kCStages = 3;      // staged code tiles (run ahead of the dequant)
 constexpr int kCK = 256;         // K of one code stage: 128-byte row pieces (whole lines)
 constexpr int kBoxRows = 32;     // TMA box: 32 rows x 64 bf16
