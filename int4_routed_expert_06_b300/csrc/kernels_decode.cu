@@ -98,7 +98,10 @@ cudaError_t launch_router(const Shape &s, const void *x, int T, const void *w_ro
                           const float *bias, const void *w_sg, float *logits, float *sg_logit,
                           cudaStream_t st)
 {
-    if (router_gemm_eligible(s, T))
+    // the tensor-core GEMM reads x and the router rows through TMA and the
+    // shared-gate row with 16-byte loads
+    const auto a16 = [](const void *p) { return ((uintptr_t)p & 15u) == 0; };
+    if (router_gemm_eligible(s, T) && a16(x) && a16(w_router) && a16(w_sg))
         return launch_router_gemm(s, x, T, w_router, bias, w_sg, logits, sg_logit, st);
     if (s.act == MOE_BF16 && s.router == MOE_BF16)
         return router_dispatch<__nv_bfloat16, __nv_bfloat16>(s, x, T, w_router, bias, w_sg, logits, sg_logit, st);

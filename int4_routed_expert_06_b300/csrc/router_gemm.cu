@@ -1,147 +1,195 @@
-// Router logits of many tokens as one dense GEMM on the tensor cores.
+// Router logits of many tokens as one dense GEMM on the 5th-generation tensor
+// cores.
 //
-// For T tokens the router is logits[T, E] = x[T, H] . w_router[E, H]^T + b,
-// together with the shared-gate logit sg[T] = x[T, H] . w_sg[H]: one bf16 GEMM
-// against E + 1 weight rows (8.6 GFLOP for a 4096-token 80B prefill), fp32
-// accumulation.  CTA tile 128 tokens x 128 weight rows, K steps of 32, staged
-// in shared memory by cp.async (two stages, rows padded to 40 elements so
-// that every ldmatrix phase is free of bank conflicts), 8 warps of 64 x 32 each
-// on mma.sync m16n8k16.  The epilogue adds the bias and writes weight row E to
-// sg.
+// For T tokens the router is logits[T, E] = x[T, H] . w_router[E, H]^T + b
+// (8.6 GFLOP for a 4096-token 80B prefill), bf16 operands, fp32 accumulation
+// in TMEM.  CTA tile: 128 tokens x 128 router rows; K in 64-column steps (one
+// 128-byte swizzle atom of bf16), both operands brought in by TMA into a
+// 4-stage ring; one thread issues tcgen05.mma (M = 128, N = 128, K = 16)
+// and commits each stage back to the producer; after the last stage the
+// four warps read the accumulator out of TMEM, add the bias and write the
+// logits.  The shared-gate logit sg[T] = x[T, H] . w_sg[H] is a warp-per-token
+// GEMV beside it.  (This file is included after prefill.cu in the library's
+// single translation unit and uses its TMA, mbarrier and TMEM helpers.)
 #include "internal.h"
 
 namespace moe {
 namespace rgemm {
 
-constexpr int BM = 128, BN = 128, BK = 32, LDS = BK + 8; // smem row: 40 bf16 = 80 B
-constexpr int kThreads = 256;
+constexpr int TBM = 128, TBN = 128, TBK = 64, TST = 4;
+constexpr int kThreads = 128;
+constexpr uint32_t kTileA = TBM * TBK * 2; // 16 KB
+constexpr uint32_t kTileB = TBN * TBK * 2; // 16 KB
+constexpr uint32_t kSmem = TST * (kTileA + kTileB) + 1024;
 
-__device__ __forceinline__ uint32_t saddr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-// 16-byte copy global -> shared, zero-filled when `valid` is false.
-__device__ __forceinline__ void cp16z(void *dst, const void *src, bool valid)
+// D (TMEM) += A . B, both K-major in shared memory (128-byte swizzle).
+__device__ __forceinline__ void mma_ss(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate)
 {
-    const int n = valid ? 16 : 0;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(saddr(dst)), "l"(src), "r"(n) : "memory");
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+                 : "memory");
 }
 
-__device__ __forceinline__ void ldsm_x4(const void *p, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
+__global__ void __launch_bounds__(kThreads, 1)
+    router_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mw, int T, int E,
+                     int K, const float *__restrict__ bias, float *__restrict__ logits)
 {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(saddr(p)));
-}
+    using namespace prefill;
+    extern __shared__ unsigned char smem_raw[];
+    __shared__ uint64_t full[TST], empty[TST], done;
+    __shared__ uint32_t tmem_base;
+    __shared__ volatile int s_fail;
+    const uint32_t raw = smem_u32(smem_raw);
+    unsigned char *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    unsigned char *a_tiles = smem, *b_tiles = smem + TST * kTileA;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * TBM, n0 = blockIdx.y * TBN, nk = K / TBK;
 
-__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
-{
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-                 "{%8, %9}, {%0, %1, %2, %3};"
-                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Weight row n of the router-plus-shared-gate matrix (E rows, then w_sg).
-__device__ __forceinline__ const __nv_bfloat16 *wrow(const __nv_bfloat16 *wr, const __nv_bfloat16 *wsg, int n,
-                                                     int E, int H)
-{
-    return n < E ? wr + (size_t)n * H : wsg;
-}
-
-__global__ void __launch_bounds__(kThreads) router_gemm_kernel(const __nv_bfloat16 *__restrict__ x, int T, int H,
-                                                               int E, const __nv_bfloat16 *__restrict__ wr,
-                                                               const __nv_bfloat16 *__restrict__ wsg,
-                                                               const float *__restrict__ bias,
-                                                               float *__restrict__ logits, float *__restrict__ sg)
-{
-    __shared__ __align__(128) __nv_bfloat16 As[2][BM][LDS];
-    __shared__ __align__(128) __nv_bfloat16 Bs[2][BN][LDS];
-    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
-    const int N = E + (wsg ? 1 : 0);
-    const int wm = (warp >> 2) * 64, wn = (warp & 3) * 32; // warp tile origin in the CTA tile
-
-    // stage K step kk into buffer b: 128 rows x 4 pieces of 16 B, for A and B
-    auto stage = [&](int b, int kk) {
-        for (int p = t; p < BM * 4; p += kThreads) {
-            const int r = p >> 2, c = (p & 3) * 8;
-            const int m = m0 + r, n = n0 + r;
-            cp16z(&As[b][r][c], x + (size_t)min(m, T - 1) * H + kk + c, m < T);
-            cp16z(&Bs[b][r][c], wrow(wr, wsg, min(n, N - 1), E, H) + kk + c, n < N);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < TST; ++s) {
+            bar_init(&full[s], 1);
+            bar_init(&empty[s], 1);
         }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-    };
-
-    float acc[4][4][4] = {}; // [m16 tile][n8 tile][fragment]
-    const int nk = H / BK;
-    stage(0, 0);
-    for (int ks = 0; ks < nk; ++ks) {
-        const int b = ks & 1;
-        if (ks + 1 < nk)
-            stage(b ^ 1, (ks + 1) * BK);
-        else
-            asm volatile("cp.async.commit_group;" ::: "memory");
-        asm volatile("cp.async.wait_group 1;" ::: "memory");
-        __syncthreads();
-#pragma unroll
-        for (int k16 = 0; k16 < BK; k16 += 16) {
-            uint32_t a[4][4], bf[2][4];
-            const int q = lane >> 3, rr = lane & 7;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                ldsm_x4(&As[b][wm + 16 * i + rr + 8 * (q & 1)][k16 + 8 * (q >> 1)], a[i][0], a[i][1], a[i][2],
-                        a[i][3]);
-#pragma unroll
-            for (int jj = 0; jj < 2; ++jj) // n8 tiles 2 jj and 2 jj + 1
-                ldsm_x4(&Bs[b][wn + 16 * jj + rr + 8 * (q >> 1)][k16 + 8 * (q & 1)], bf[jj][0], bf[jj][1],
-                        bf[jj][2], bf[jj][3]);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    mma_bf16(acc[i][j], a[i], bf[j >> 1][2 * (j & 1)], bf[j >> 1][2 * (j & 1) + 1]);
-        }
-        __syncthreads(); // buffer b is restaged by the next iteration's copies
+        bar_init(&done, 1);
+        s_fail = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 128;" ::"r"(smem_u32(&tmem_base))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
 
-    // epilogue: fragment c0, c1 = (row g, cols 2u, 2u + 1), c2, c3 = row g + 8
-    const int g = lane >> 2, u = lane & 3;
+    if (warp == 0 && lane == 0) {
+        // ---- TMA producer: x rows [m0, m0 + 128) and router rows [n0, n0 + 128)
+        // (rows past T or E read as zero)
+        for (int k = 0; k < nk; ++k) {
+            const int s = k % TST;
+            if (!bar_wait(&empty[s], ((k / TST) & 1) ^ 1)) {
+                s_fail = 1;
+                break;
+            }
+            bar_expect(&full[s], kTileA + kTileB);
+            tma_load_2d(a_tiles + s * kTileA, &mx, k * TBK, m0, &full[s]);
+            tma_load_2d(b_tiles + s * kTileB, &mw, k * TBK, n0, &full[s]);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer
+        const uint32_t idesc = idesc_bf16(TBM, TBN);
+        for (int k = 0; k < nk; ++k) {
+            const int s = k % TST;
+            if (!bar_wait(&full[s], (k / TST) & 1)) {
+                s_fail = 1;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t a = smem_u32(a_tiles + s * kTileA), b = smem_u32(b_tiles + s * kTileB);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+            for (int kk = 0; kk < TBK / 16; ++kk)
+                mma_ss(tmem, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), idesc, (k > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&empty[s]);
+        }
+        mma_commit(&done);
+    }
+    __syncwarp();
+    // ---- epilogue: warp w reads TMEM lanes 32 w .. + 31 (tokens), 128 columns
+    const bool ok = __all_sync(0xFFFFFFFFu, bar_wait(&done, 0) && !s_fail); // tcgen05.ld is warp-collective
+    tc_fence_after();
+    const int m = m0 + warp * 32 + lane;
+    if (ok) {
+        for (int c0 = 0; c0 < TBN; c0 += 16) {
+            uint32_t v[16];
+            tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+            if (m < T) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int m = m0 + wm + 16 * i + g + 8 * h;
-                if (m >= T)
-                    continue;
-#pragma unroll
-                for (int v = 0; v < 2; ++v) {
-                    const int n = n0 + wn + 8 * j + 2 * u + v;
-                    const float val = acc[i][j][2 * h + v];
+                for (int j = 0; j < 16; ++j) {
+                    const int n = n0 + c0 + j;
                     if (n < E)
-                        logits[(size_t)m * E + n] = val + (bias ? bias[n] : 0.f);
-                    else if (n == E && wsg)
-                        sg[m] = val;
+                        logits[(size_t)m * E + n] = __uint_as_float(v[j]) + (bias ? bias[n] : 0.f);
                 }
             }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 128;" ::"r"(tmem) : "memory");
+    }
+}
+
+// sg[t] = x[t] . w_sg, one warp a token, fp32 accumulation (H a multiple of 8).
+__global__ void __launch_bounds__(256) shared_gate_kernel(const __nv_bfloat16 *__restrict__ x,
+                                                          const __nv_bfloat16 *__restrict__ w, int T, int H,
+                                                          float *__restrict__ sg)
+{
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (t >= T)
+        return;
+    const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)t * H), *wr = reinterpret_cast<const uint4 *>(w);
+    float acc = 0.f;
+    for (int c = lane; c < H / 8; c += 32) {
+        const uint4 a = __ldg(xr + c), b = __ldg(wr + c);
+        const uint32_t aa[4] = {a.x, a.y, a.z, a.w}, bb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            acc = fmaf(__uint_as_float(aa[j] << 16), __uint_as_float(bb[j] << 16), acc);
+            acc = fmaf(__uint_as_float(aa[j] & 0xFFFF0000u), __uint_as_float(bb[j] & 0xFFFF0000u), acc);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+    if (lane == 0)
+        sg[t] = acc;
+}
+
+// 2-D map over a row-major bf16 matrix [rows, cols]: boxes of `box_rows` rows
+// x 64 columns, 128-byte swizzle.
+static bool make_map_rows(CUtensorMap *m, const void *base, long rows, int cols, int box_rows)
+{
+    prefill::EncodeTiledFn fn = prefill::encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)TBK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 } // namespace rgemm
 
 bool router_gemm_eligible(const Shape &s, int T)
 {
-    return T >= kRouterGemmMinTokens && s.act == MOE_BF16 && s.router == MOE_BF16 && s.H % rgemm::BK == 0 &&
-           kernel_path() != 1;
+    return T >= kRouterGemmMinTokens && s.act == MOE_BF16 && s.router == MOE_BF16 && s.H % rgemm::TBK == 0 &&
+           kernel_path() != 1 && prefill::encode_fn() != nullptr;
 }
 
 cudaError_t launch_router_gemm(const Shape &s, const void *x, int T, const void *w_router, const float *bias,
                                const void *w_sg, float *logits, float *sg_logit, cudaStream_t st)
 {
-    const int N = s.E + (w_sg ? 1 : 0);
-    const dim3 grid((T + rgemm::BM - 1) / rgemm::BM, (N + rgemm::BN - 1) / rgemm::BN);
-    rgemm::router_gemm_kernel<<<grid, rgemm::kThreads, 0, st>>>(
-        static_cast<const __nv_bfloat16 *>(x), T, s.H, s.E, static_cast<const __nv_bfloat16 *>(w_router),
-        static_cast<const __nv_bfloat16 *>(w_sg), bias, logits, sg_logit);
+    CUtensorMap mx, mw;
+    if (!rgemm::make_map_rows(&mx, x, T, s.H, rgemm::TBM) || !rgemm::make_map_rows(&mw, w_router, s.E, s.H, rgemm::TBN))
+        return cudaErrorInvalidValue;
+    static int cur = 0;
+    cudaError_t e = ensure_smem(rgemm::router_tc_kernel, rgemm::kSmem, &cur);
+    if (e != cudaSuccess)
+        return e;
+    const dim3 grid((T + rgemm::TBM - 1) / rgemm::TBM, (s.E + rgemm::TBN - 1) / rgemm::TBN);
+    rgemm::router_tc_kernel<<<grid, rgemm::kThreads, rgemm::kSmem, st>>>(mx, mw, T, s.E, s.H, bias, logits);
+    if (w_sg && sg_logit)
+        rgemm::shared_gate_kernel<<<(T + 7) / 8, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(x),
+                                                               static_cast<const __nv_bfloat16 *>(w_sg), T, s.H,
+                                                               sg_logit);
     return cudaGetLastError();
 }
 
