@@ -178,6 +178,27 @@ __device__ __forceinline__ void mma_bf16_ta(uint32_t tmem_d, uint32_t tmem_a, ui
                  : "memory");
 }
 
+// The same MMA (and below, the same commit) issued by one lane of a
+// converged warp: elect.sync picks the lowest active lane, so a warp that
+// runs with all lanes always issues from lane 0, and a commit tracks the
+// MMAs that lane issued.
+__device__ __forceinline__ void mma_bf16_ta_elect(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                                  uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+                 "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_elect(uint64_t *bar)
+{
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -657,50 +678,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issuer
-        if (lane == 0) {
-            int stage = 0, acc = 0;
-            uint32_t ph = 0, acc_ph = 0;
-            Unit u = blockIdx.x < nu ? A.units[blockIdx.x] : Unit{};
-            for (int ui = blockIdx.x; ui < nu && !s_abort; ui += grid) {
-                const Unit nx = next_unit(ui, u);
-                const int K = kdim(u);
-                const int N = (u.n + 15) & ~15;
-                const uint32_t idesc = idesc_bf16(128, N);
-                const uint32_t d_tmem = tmem + (uint32_t)acc * kAccCols;
-                if (!bar_wait(&acc_empty[acc], acc_ph ^ 1)) {
+        // The whole warp runs the loop, so that every MMA operand is
+        // warp-uniform, and one elected lane (the same one throughout)
+        // issues each tcgen05.mma and commit.  The B descriptors are formed
+        // once: a stage and a 16-column step only add a constant to the start
+        // address field.
+        int stage = 0, acc = 0;
+        uint32_t ph = 0, acc_ph = 0;
+        const uint64_t bdesc0 = sw128_desc(smem_u32(b_tiles));
+        Unit u = blockIdx.x < nu ? A.units[blockIdx.x] : Unit{};
+        for (int ui = blockIdx.x; ui < nu; ui += grid) {
+            if (__any_sync(0xFFFFFFFFu, s_abort))
+                break;
+            const Unit nx = next_unit(ui, u);
+            const int K = kdim(u);
+            const int N = (u.n + 15) & ~15;
+            const uint32_t idesc = idesc_bf16(128, N);
+            const uint32_t d_tmem = tmem + (uint32_t)acc * kAccCols;
+            if (!__all_sync(0xFFFFFFFFu, bar_wait(&acc_empty[acc], acc_ph ^ 1))) {
+                s_abort = 1;
+                break;
+            }
+            tc_fence_after();
+            bool fail = false;
+            for (int k0 = 0; k0 < K; k0 += kBK) {
+                if (!__all_sync(0xFFFFFFFFu, bar_wait(&a_full[stage], ph) && bar_wait(&b_full[stage], ph))) {
                     s_abort = 1;
+                    fail = true;
                     break;
                 }
                 tc_fence_after();
-                for (int k0 = 0; k0 < K; k0 += kBK) {
-                    if (!bar_wait(&a_full[stage], ph) || !bar_wait(&b_full[stage], ph)) {
-                        s_abort = 1;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t a_t = tmem + kACol0 + (uint32_t)stage * kACols;
-                    const uint32_t b_addr = smem_u32(b_tiles + stage * kBTile);
+                const uint32_t a_t = tmem + kACol0 + (uint32_t)stage * kACols;
+                const uint64_t bd = bdesc0 + (uint64_t)(stage * (kBTile >> 4));
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) { // B atom kk / 4, 16-column step kk % 4 within it
-                        const uint32_t bo = (uint32_t)(kk / 4) * (kNch * 128) + (uint32_t)(kk % 4) * 32;
-                        mma_bf16_ta(d_tmem, a_t + (uint32_t)kk * 8, sw128_desc(b_addr + bo), idesc,
-                                    (k0 > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    mma_commit(&ab_empty[stage]);
-                    if (++stage == kStages) {
-                        stage = 0;
-                        ph ^= 1;
-                    }
+                for (int kk = 0; kk < kBK / 16; ++kk) { // B atom kk / 4, 16-column step kk % 4 within it
+                    const uint32_t bo = (uint32_t)(kk / 4) * (kNch * 128) + (uint32_t)(kk % 4) * 32;
+                    mma_bf16_ta_elect(d_tmem, a_t + (uint32_t)kk * 8, bd + (bo >> 4), idesc,
+                                      (k0 > 0 || kk > 0) ? 1u : 0u);
                 }
-                if (s_abort)
-                    break;
-                mma_commit(&acc_full[acc]);
-                if (++acc == 2) {
-                    acc = 0;
-                    acc_ph ^= 1;
+                mma_commit_elect(&ab_empty[stage]);
+                if (++stage == kStages) {
+                    stage = 0;
+                    ph ^= 1;
                 }
-                u = nx;
             }
+            if (fail)
+                break;
+            mma_commit_elect(&acc_full[acc]);
+            if (++acc == 2) {
+                acc = 0;
+                acc_ph ^= 1;
+            }
+            u = nx;
         }
     } else {
         // ---------------- epilogue: 4 warps, TMEM lanes 32*(warp%4) ..

@@ -5,10 +5,10 @@
 // (8.6 GFLOP for a 4096-token 80B prefill), bf16 operands, fp32 accumulation
 // in TMEM.  CTA tile: 128 tokens x 128 router rows; K in 64-column steps (one
 // 128-byte swizzle atom of bf16), both operands brought in by TMA into a
-// 4-stage ring; one thread issues tcgen05.mma (M = 128, N = 128, K = 16)
-// and commits each stage back to the producer; after the last stage the
-// four warps read the accumulator out of TMEM, add the bias and write the
-// logits.  The shared-gate logit sg[T] = x[T, H] . w_sg[H] is a warp-per-token
+// 4-stage ring; one elected lane of the MMA warp issues tcgen05.mma (M = 128,
+// N = 128, K = 16) and commits each stage back to the producer; after the
+// last stage the four warps read the accumulator out of TMEM, add the bias
+// and write the logits.  The shared-gate logit sg[T] = x[T, H] . w_sg[H] is a warp-per-token
 // GEMV beside it.  (This file is included after prefill.cu in the library's
 // single translation unit and uses its TMA, mbarrier and TMEM helpers.)
 #include "internal.h"
@@ -22,12 +22,13 @@ constexpr uint32_t kTileA = TBM * TBK * 2; // 16 KB
 constexpr uint32_t kTileB = TBN * TBK * 2; // 16 KB
 constexpr uint32_t kSmem = TST * (kTileA + kTileB) + 1024;
 
-// D (TMEM) += A . B, both K-major in shared memory (128-byte swizzle).
-__device__ __forceinline__ void mma_ss(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                       uint32_t accumulate)
+// D (TMEM) += A . B, both K-major in shared memory (128-byte swizzle), issued
+// by the elected lane of a converged warp.
+__device__ __forceinline__ void mma_ss_elect(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate)
 {
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+    asm volatile("{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
                  "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
                  : "memory");
 }
@@ -79,23 +80,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(a_tiles + s * kTileA, &mx, k * TBK, m0, &full[s]);
             tma_load_2d(b_tiles + s * kTileB, &mw, k * TBK, n0, &full[s]);
         }
-    } else if (warp == 1 && lane == 0) {
-        // ---- MMA issuer
+    } else if (warp == 1) {
+        // ---- MMA issuer: the whole warp runs the loop (operands warp-uniform),
+        // one elected lane issues; descriptors formed once, then offset
         const uint32_t idesc = idesc_bf16(TBM, TBN);
+        const uint64_t ad0 = sw128_desc(smem_u32(a_tiles)), bd0 = sw128_desc(smem_u32(b_tiles));
         for (int k = 0; k < nk; ++k) {
             const int s = k % TST;
-            if (!bar_wait(&full[s], (k / TST) & 1)) {
+            if (!__all_sync(0xFFFFFFFFu, bar_wait(&full[s], (k / TST) & 1))) {
                 s_fail = 1;
                 break;
             }
             tc_fence_after();
-            const uint32_t a = smem_u32(a_tiles + s * kTileA), b = smem_u32(b_tiles + s * kTileB);
+            const uint64_t ad = ad0 + (uint64_t)(s * (kTileA >> 4)), bd = bd0 + (uint64_t)(s * (kTileB >> 4));
 #pragma unroll
             for (int kk = 0; kk < TBK / 16; ++kk)
-                mma_ss(tmem, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), idesc, (k > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(&empty[s]);
+                mma_ss_elect(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (k > 0 || kk > 0) ? 1u : 0u);
+            mma_commit_elect(&empty[s]);
         }
-        mma_commit(&done);
+        mma_commit_elect(&done);
     }
     __syncwarp();
     // ---- epilogue: warp w reads TMEM lanes 32 w .. + 31 (tokens), 128 columns
