@@ -96,6 +96,23 @@ __device__ __forceinline__ bool bar_try(uint64_t *b, uint32_t parity)
     return ok != 0;
 }
 
+// The same test, but a thread whose phase has not completed is suspended
+// until it completes or about `hint_ns` nanoseconds have passed, instead of
+// returning at once: a waiting warp then takes no issue slots from the warps
+// that share its scheduler.
+__device__ __forceinline__ bool bar_try_suspend(uint64_t *b, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_u32(b)), "r"(parity), "r"(hint_ns)
+                 : "memory");
+    return ok != 0;
+}
+
+constexpr uint32_t kSuspendNs = 20u * 1000; // one suspended test: well inside kWaitNs
+
 // Wait until the phase of parity `parity` has completed, for at most kWaitNs.
 __device__ __forceinline__ bool bar_wait(uint64_t *b, uint32_t parity)
 {
@@ -103,9 +120,8 @@ __device__ __forceinline__ bool bar_wait(uint64_t *b, uint32_t parity)
         return true;
     const uint64_t t0 = gtime();
     for (;;) {
-        for (int i = 0; i < 32; ++i)
-            if (bar_try(b, parity))
-                return true;
+        if (bar_try_suspend(b, parity, kSuspendNs))
+            return true;
         if (gtime() - t0 > kWaitNs) {
             record_error(MOE_ERR_TIMEOUT);
             return false;
@@ -491,6 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // failed wait sets s_dq_fail, and the decision to stop is read after
         // the next dq_sync.
         const int t = threadIdx.x, qd = warp & 3, part = warp >> 2, r = qd * 32 + lane;
+        const int gshift = (G & (G - 1)) == 0 ? __ffs(G) - 1 : -1; // group size a power of two: shift, not divide
         const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16) + kACol0 + (uint32_t)part * (kACols / 4);
         int cs = 0, as = 0;
         uint32_t cph = 0, aph = 0, sph = 0;
@@ -512,8 +529,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             {
                 const TS *raw = reinterpret_cast<const TS *>(s_raw);
+                // a warp takes 32 rows of one pass j, row rr its group
+                // (j + rot(rr)) mod ng: each row still visits every group once,
+                // but the lanes' 2-byte reads of the row-major scale rows now
+                // spread over the banks (at most 2-way conflicts for 8, 16 or
+                // 32 groups; with one group a warp they were 4- to 16-way), and
+                // the pair writes, one row a lane, stay conflict-free
+                // (a thread's row rr = t mod 128 is the same on every pass)
+                static_assert((kDqWarps * 32) % 128 == 0, "one row a thread across the passes");
+                const int rot = ((t & 127) >> 1) + (((t & 127) >> 4) << 1), rot_ng = rot % ng;
                 for (int e = t; e < 128 * ng; e += kDqWarps * 32) {
-                    const int g = e >> 7, rr = e & 127;
+                    const int j = e >> 7, rr = e & 127;
+                    const int g = j + rot_ng < ng ? j + rot_ng : j + rot_ng - ng;
                     int si, bi;
                     if (A.mode == 0) { // raw: sg, bg, su, bu, each [64 rows][ng]; rows interleave gate / up
                         const int m = rr & 1, f = rr >> 1;
@@ -523,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         si = rr * ng + g;
                         bi = si + 128 * ng;
                     }
-                    s_pair[e] = SBPair<TS>{raw[si], raw[bi]};
+                    s_pair[g * 128 + rr] = SBPair<TS>{raw[si], raw[bi]};
                 }
             }
             dq_sync(); // the pairs are complete and the raw rows free
@@ -553,7 +580,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (ok) {
                         const int c16 = ((k0 - kc) >> 5) + part; // 16-byte chunk of the row piece
                         const uint4 qw = *reinterpret_cast<const uint4 *>(cp + ((c16 ^ (brow & 7)) << 4));
-                        const SBPair<TS> p = s_pair[((k0 + 32 * part) / G) * 128 + r];
+                        const int kp = k0 + 32 * part, gi = gshift >= 0 ? kp >> gshift : kp / G;
+                        const SBPair<TS> p = s_pair[gi * 128 + r];
                         dequant_32(qw, to_f32(p.s), to_f32(p.b), packed);
                     } else {
 #pragma unroll
