@@ -322,19 +322,26 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
         *n_units = total;
 }
 
-// y[t, h] = sum_r P[inv[t, r], h] + P[T*k + t, h]; bf16 y and optional fp32,
-// one output a thread (any alignment of y and y32).
-__global__ void combine_scalar_kernel(const float *__restrict__ P, const int32_t *__restrict__ inv, int T, int k,
-                                      int H, int has_shared, __nv_bfloat16 *__restrict__ y, float *__restrict__ y32)
+// y[t, h] = sum_r w[p] P[p, h] with p = inv[t, r], + w[T*k + t] P[T*k + t, h]:
+// the routing weight of each pair (and the shared expert's gate) times its
+// down-projection row, each product rounded to fp32 and summed in rank order;
+// bf16 y and optional fp32, one output a thread (any alignment of y and y32).
+__global__ void combine_scalar_kernel(const float *__restrict__ P, const float *__restrict__ wpair,
+                                      const int32_t *__restrict__ inv, int T, int k, int H, int has_shared,
+                                      __nv_bfloat16 *__restrict__ y, float *__restrict__ y32)
 {
     const long n = (long)T * H;
     for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
         const int t = (int)(i / H), h = (int)(i - (long)t * H);
         float acc = 0.f;
-        for (int r = 0; r < k; ++r)
-            acc += __ldg(P + (long)inv[t * k + r] * H + h);
-        if (has_shared)
-            acc += __ldg(P + ((long)T * k + t) * H + h);
+        for (int r = 0; r < k; ++r) {
+            const int p = inv[t * k + r];
+            acc += __fmul_rn(__ldg(wpair + p), __ldg(P + (long)p * H + h));
+        }
+        if (has_shared) {
+            const long p = (long)T * k + t;
+            acc += __fmul_rn(__ldg(wpair + p), __ldg(P + p * H + h));
+        }
         y[i] = __float2bfloat16_rn(acc);
         if (y32)
             y32[i] = acc;
@@ -343,8 +350,9 @@ __global__ void combine_scalar_kernel(const float *__restrict__ P, const int32_t
 
 // The same sum in the same order, four consecutive h a thread (16-byte loads;
 // H a multiple of 4, y 8-byte and y32 16-byte aligned).
-__global__ void combine_kernel(const float *__restrict__ P, const int32_t *__restrict__ inv, int T, int k, int H,
-                               int has_shared, __nv_bfloat16 *__restrict__ y, float *__restrict__ y32)
+__global__ void combine_kernel(const float *__restrict__ P, const float *__restrict__ wpair,
+                               const int32_t *__restrict__ inv, int T, int k, int H, int has_shared,
+                               __nv_bfloat16 *__restrict__ y, float *__restrict__ y32)
 {
     const int H4 = H >> 2;
     const long n = (long)T * H4;
@@ -352,18 +360,22 @@ __global__ void combine_kernel(const float *__restrict__ P, const int32_t *__res
         const int t = (int)(i / H4), h4 = (int)(i - (long)t * H4);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int r = 0; r < k; ++r) {
-            const float4 v = __ldg(reinterpret_cast<const float4 *>(P + (long)inv[t * k + r] * H) + h4);
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
+            const int p = inv[t * k + r];
+            const float w = __ldg(wpair + p);
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(P + (long)p * H) + h4);
+            acc.x += __fmul_rn(w, v.x);
+            acc.y += __fmul_rn(w, v.y);
+            acc.z += __fmul_rn(w, v.z);
+            acc.w += __fmul_rn(w, v.w);
         }
         if (has_shared) {
-            const float4 v = __ldg(reinterpret_cast<const float4 *>(P + ((long)T * k + t) * H) + h4);
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
+            const long p = (long)T * k + t;
+            const float w = __ldg(wpair + p);
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(P + p * H) + h4);
+            acc.x += __fmul_rn(w, v.x);
+            acc.y += __fmul_rn(w, v.y);
+            acc.z += __fmul_rn(w, v.z);
+            acc.w += __fmul_rn(w, v.w);
         }
         __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
         uint2 packed;
@@ -384,9 +396,9 @@ struct GemmArgs {
     int mode;            // 0 gate/up, 1 down
     int H, I, Is, G, T, k;
     int act_ld;          // row length of the activation buffer (max(I, Is))
-    const float *wpair;  // down: weight of each sorted row
+    const float *wpair;  // weight of each sorted row (applied by the combine)
     __nv_bfloat16 *act;  // gate/up output [T*k + T, act_ld]
-    float *pout;         // down output [T*k + T, H]
+    float *pout;         // down output [T*k + T, H], unweighted
 };
 
 // Tensor maps of the weight side of one GEMM kind, over the fixed-stride
@@ -779,25 +791,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t v[16];
                 tmem_ld16(t_row + (uint32_t)c0, v);
                 if (A.mode == 0) {
+                    // rows 2f (gate) and 2f + 1 (up) of feature f sit in a lane
+                    // pair: the even lane finishes column j, the odd lane
+                    // column j + 1, each with one exchange
                     const int f = u.ft * 64 + (r >> 1);
+                    const bool odd = r & 1;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float mine = __uint_as_float(v[j]);
-                        const float other = __shfl_xor_sync(0xFFFFFFFFu, mine, 1);
-                        if (!(r & 1) && c0 + j < u.n) {
-                            const float g = mine, up = other;
+                    for (int j = 0; j < 16; j += 2) {
+                        const float c_j = __uint_as_float(v[j]), c_j1 = __uint_as_float(v[j + 1]);
+                        const float got = __shfl_xor_sync(0xFFFFFFFFu, odd ? c_j : c_j1, 1);
+                        const float g = odd ? got : c_j, up = odd ? c_j1 : got;
+                        const int col = c0 + j + (odd ? 1 : 0);
+                        if (col < u.n) {
                             const float a = g / (1.f + __expf(-g)) * up;
-                            A.act[(size_t)(rowb + c0 + j) * A.act_ld + f] = __float2bfloat16_rn(a);
+                            A.act[(size_t)(rowb + col) * A.act_ld + f] = __float2bfloat16_rn(a);
                         }
                     }
                 } else {
+                    // the routing weight is applied by the combine
                     const int h = u.ft * 128 + r;
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        if (c0 + j < u.n) {
-                            const int row = rowb + c0 + j;
-                            A.pout[(size_t)row * A.H + h] = A.wpair[row] * __uint_as_float(v[j]);
-                        }
+                        if (c0 + j < u.n)
+                            A.pout[(size_t)(rowb + c0 + j) * A.H + h] = __uint_as_float(v[j]);
                 }
             }
             tc_fence_before();
@@ -1053,10 +1069,10 @@ cudaError_t experts_forward(const Shape &s, const ExpertSrc &src, const void *x,
     if (e != cudaSuccess)
         return e;
     if ((reinterpret_cast<uintptr_t>(y) & 7) == 0 && (reinterpret_cast<uintptr_t>(y32) & 15) == 0)
-        combine_kernel<<<4 * sm_count(), 256, 0, st>>>(pout, inv, T, s.k, s.H, 1, static_cast<__nv_bfloat16 *>(y),
-                                                        y32);
+        combine_kernel<<<4 * sm_count(), 256, 0, st>>>(pout, wpair, inv, T, s.k, s.H, 1,
+                                                        static_cast<__nv_bfloat16 *>(y), y32);
     else
-        combine_scalar_kernel<<<4 * sm_count(), 256, 0, st>>>(pout, inv, T, s.k, s.H, 1,
+        combine_scalar_kernel<<<4 * sm_count(), 256, 0, st>>>(pout, wpair, inv, T, s.k, s.H, 1,
                                                                static_cast<__nv_bfloat16 *>(y), y32);
     return cudaGetLastError();
 }
