@@ -220,14 +220,17 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 
 // ------------------------------------------------------------ small kernels
 
-// X_sorted[p] = x[perm_tok[p]], rows of H bf16 (16-byte copies).
+// X_sorted[p] = x[perm_tok[p]], rows of H bf16: a warp a row, its lanes over
+// the row's 16-byte chunks (no index division).
 __global__ void gather_rows_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ perm_tok, int P,
                                    int row16, uint4 *__restrict__ xs)
 {
-    const long n = (long)P * row16;
-    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
-        const long p = i / row16, c = i - p * row16;
-        xs[i] = __ldg(x + (long)perm_tok[p] * row16 + c);
+    const int lane = threadIdx.x & 31, wpb = blockDim.x >> 5;
+    for (int p = blockIdx.x * wpb + (threadIdx.x >> 5); p < P; p += gridDim.x * wpb) {
+        const uint4 *src = x + (long)perm_tok[p] * row16;
+        uint4 *dst = xs + (long)p * row16;
+        for (int c = lane; c < row16; c += 32)
+            dst[c] = __ldg(src + c);
     }
 }
 
@@ -249,39 +252,51 @@ __global__ void pair_prep_kernel(const int32_t *__restrict__ perm_tok, const int
     }
 }
 
-// One CTA: rank the experts by token count (descending, ties by id), lay out
-// their units in that order after the shared expert's.  Unit order within an
-// expert: token chunk major, feature tile minor.  E <= 1024.
+// Units of both GEMM kinds from one ranking.  Every CTA ranks the experts by
+// token count (descending, ties by id: a bitonic sort of 64-bit keys in
+// shared memory) and scans their token chunks of up to kNch tokens; CTA b then
+// writes units b, b + grid, ... of each list: the shared expert's first, then
+// the experts' in rank order, token chunk major and feature tile minor within
+// an expert.  The unit count of a kind is n_ft x chunks, so one chunk scan
+// serves both kinds.  E <= 1024.
+constexpr int kPlanCtas = 16;
+
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ counts,
                                                     const int32_t *__restrict__ offsets,
                                                     const int32_t *__restrict__ table, int n_slots, int E, int T,
-                                                    int n_ft, int n_ft_sh, int has_shared, Unit *__restrict__ units,
+                                                    int n_ft0, int n_ft_sh0, int n_ft1, int n_ft_sh1, int has_shared,
+                                                    Unit *__restrict__ units0, Unit *__restrict__ units1,
                                                     int32_t *__restrict__ n_units)
 {
-    __shared__ int s_cnt[1024];
-    __shared__ int s_ord[1024];
-    __shared__ int s_scan[1024];
-    __shared__ int s_slot[1024]; // by rank position: the expert's slot
+    __shared__ unsigned long long s_key[1024];
+    __shared__ int s_ord[1024];  // expert at each rank position
+    __shared__ int s_scan[1024]; // inclusive scan of token chunks by rank position
+    __shared__ int s_slot[1024]; // slot of the expert at each rank position
     const int e = threadIdx.x;
-    s_cnt[e] = e < E ? counts[e] : -1;
+    // ascending keys = (count descending, id ascending); past E: the largest key
+    s_key[e] = e < E ? ((unsigned long long)(0x7FFFFFFF - counts[e]) << 32) | (unsigned)e : ~0ull;
     __syncthreads();
-    int rank = 0;
-    if (e < E) {
-        const int c = s_cnt[e];
-        for (int j = 0; j < E; ++j) {
-            const int cj = s_cnt[j];
-            rank += (cj > c || (cj == c && j < e)) ? 1 : 0;
+    for (int k = 2; k <= 1024; k <<= 1)
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const int ixj = e ^ j;
+            if (ixj > e) {
+                const unsigned long long a = s_key[e], b = s_key[ixj];
+                if ((a > b) == ((e & k) == 0)) {
+                    s_key[e] = b;
+                    s_key[ixj] = a;
+                }
+            }
+            __syncthreads();
         }
-        s_ord[rank] = e;
-    }
-    __syncthreads();
-    // units of the expert at rank position e
-    int nu = 0, ex = -1;
+    int ch = 0, ex = -1;
     if (e < E) {
-        ex = s_ord[e];
-        nu = n_ft * ((s_cnt[ex] + kNch - 1) / kNch);
+        ex = (int)(s_key[e] & 0xFFFFFFFFu);
+        ch = (counts[ex] + kNch - 1) / kNch;
+        const int sl = table[ex];
+        s_slot[e] = sl >= 0 && sl < n_slots ? sl : -1;
     }
-    s_scan[e] = nu;
+    s_ord[e] = ex;
+    s_scan[e] = ch;
     __syncthreads();
     for (int o = 1; o < 1024; o <<= 1) { // inclusive scan (Hillis-Steele)
         const int v = e >= o ? s_scan[e - o] : 0;
@@ -289,37 +304,34 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
         s_scan[e] += v;
         __syncthreads();
     }
-    if (e < E) {
-        const int sl = table[ex];
-        s_slot[e] = sl >= 0 && sl < n_slots ? sl : -1;
-    }
-    __syncthreads();
-    // every unit written by the CTA together: unit u -> (expert at rank p,
-    // token chunk, feature tile), chunk major within an expert
-    const int n_ch_sh = has_shared ? (T + kNch - 1) / kNch : 0;
-    const int sh_units = n_ft_sh * n_ch_sh;
-    const int total = sh_units + s_scan[1023];
-    for (int u = e; u < total; u += blockDim.x) {
-        if (u < sh_units) {
-            const int c = u / n_ft_sh, ft = u - c * n_ft_sh;
-            units[u] = {-1, ft, c * kNch, min(kNch, T - c * kNch), 0};
-        } else {
-            const int v = u - sh_units;
-            int lo = 0, hi = E - 1; // first rank position p with s_scan[p] > v
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (s_scan[mid] > v)
-                    hi = mid;
-                else
-                    lo = mid + 1;
+    const int n_ch_sh = has_shared ? (T + kNch - 1) / kNch : 0, chunks = s_scan[1023];
+    const int gt = blockIdx.x * blockDim.x + e, gs = gridDim.x * blockDim.x;
+    for (int kind = 0; kind < 2; ++kind) {
+        const int n_ft = kind ? n_ft1 : n_ft0, n_ft_sh = kind ? n_ft_sh1 : n_ft_sh0;
+        Unit *units = kind ? units1 : units0;
+        const int sh_units = n_ft_sh * n_ch_sh, total = sh_units + n_ft * chunks;
+        for (int u = gt; u < total; u += gs) {
+            if (u < sh_units) {
+                const int c = u / n_ft_sh, ft = u - c * n_ft_sh;
+                units[u] = {-1, ft, c * kNch, min(kNch, T - c * kNch), 0};
+            } else {
+                const int v = u - sh_units, q = v / n_ft, ft = v - q * n_ft; // global chunk q
+                int lo = 0, hi = E - 1; // first rank position p with s_scan[p] > q
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (s_scan[mid] > q)
+                        hi = mid;
+                    else
+                        lo = mid + 1;
+                }
+                const int p = lo, ex2 = s_ord[p], cnt = counts[ex2];
+                const int c = q - (s_scan[p] - (cnt + kNch - 1) / kNch);
+                units[u] = {ex2, ft, offsets[ex2] + c * kNch, min(kNch, cnt - c * kNch), s_slot[p]};
             }
-            const int p = lo, ex2 = s_ord[p], first = s_scan[p] - n_ft * ((s_cnt[ex2] + kNch - 1) / kNch);
-            const int local = v - first, c = local / n_ft, ft = local - c * n_ft;
-            units[u] = {ex2, ft, offsets[ex2] + c * kNch, min(kNch, s_cnt[ex2] - c * kNch), s_slot[p]};
         }
+        if (blockIdx.x == 0 && e == 0)
+            n_units[kind] = total;
     }
-    if (e == 1023)
-        *n_units = total;
 }
 
 // y[t, h] = sum_r w[p] P[p, h] with p = inv[t, r], + w[T*k + t] P[T*k + t, h]:
@@ -355,9 +367,9 @@ __global__ void combine_kernel(const float *__restrict__ P, const float *__restr
                                __nv_bfloat16 *__restrict__ y, float *__restrict__ y32)
 {
     const int H4 = H >> 2;
-    const long n = (long)T * H4;
-    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
-        const int t = (int)(i / H4), h4 = (int)(i - (long)t * H4);
+    const int n = T * H4; // T <= 65536 and H <= 32768: fits 32 bits
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        const int t = i / H4, h4 = i - t * H4;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int r = 0; r < k; ++r) {
             const int p = inv[t * k + r];
@@ -1031,10 +1043,8 @@ cudaError_t experts_forward(const Shape &s, const ExpertSrc &src, const void *x,
                                                       reinterpret_cast<uint4 *>(xs));
     pair_prep_kernel<<<(int)((P + T + 255) / 256), 256, 0, st>>>(perm_tok, perm_rank, topk_w, sg, T, s.k, wpair,
                                                                  inv);
-    plan_kernel<<<1, 1024, 0, st>>>(counts, offsets, src.table, src.n_slots, s.E, T, s.I / 64, s.Is / 64, 1, u_gu,
-                                    n_units);
-    plan_kernel<<<1, 1024, 0, st>>>(counts, offsets, src.table, src.n_slots, s.E, T, s.H / 128, s.H / 128, 1, u_dn,
-                                    n_units + 1);
+    plan_kernel<<<kPlanCtas, 1024, 0, st>>>(counts, offsets, src.table, src.n_slots, s.E, T, s.I / 64, s.Is / 64,
+                                            s.H / 128, s.H / 128, 1, u_gu, u_dn, n_units);
     if ((e = cudaGetLastError()) != cudaSuccess)
         return e;
 
