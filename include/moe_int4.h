@@ -374,8 +374,9 @@ const char *moe_last_error_message(void);
 const char *moe_version(void);
 
 /* Kernel selection for calls made from the calling host thread (the setting
- * is per thread): 0 (default) uses the single-token kernels for T = 1 and
- * the tcgen05 grouped GEMMs for T >= 64 where the shape allows; 1 forces the
+ * is per thread): 0 (default) uses the single-token kernels for T = 1 (and
+ * once a token for T = 2 .. 12), the generic kernels up to T = 63 and the
+ * tcgen05 grouped GEMMs for T >= 64 where the shape allows; 1 forces the
  * generic kernels everywhere; 2 is 0 with the grouped GEMMs from T = 2 up
  * (small decode batches on the tensor cores).  All compute the same
  * function (the pages' practice of checking fast against scalar kernels);

@@ -168,18 +168,21 @@ def test_noalloc_scratch_bound_stated_in_the_header():
 
 def test_kernel_path_values_and_workspace_follow_the_path():
     """Paths 0, 1, 2 are accepted (per thread), others refused; the grouped-GEMM
-    buffers join the workspace from T = 2 under path 2 only."""
+    buffers join the workspace from T = 2 under path 2 only, and the
+    single-token buffers up to T = 12 under path 0 (the token loop)."""
     cfg = B.config_for(synth.DEC_80B)
     try:
         for bad in (-1, 3):
             with pytest.raises(B.MoEError) as ei:
                 B.moe_set_kernel_path(bad)
             assert ei.value.status == B.MOE_ERR_INVALID_ARG
-        sizes = {}
+        sizes, sizes16 = {}, {}
         for p in (0, 1, 2):
             B.moe_set_kernel_path(p)
             sizes[p] = B.moe_layer_workspace_bytes(cfg, 8)
-        assert sizes[0] == sizes[1] < sizes[2]
+            sizes16[p] = B.moe_layer_workspace_bytes(cfg, 16)
+        assert sizes[1] < sizes[0] < sizes[2]                    # T = 8: token loop on path 0
+        assert sizes16[0] == sizes16[1] < sizes16[2]             # T = 16: generic kernels on both
         B.moe_set_kernel_path(0)
         one = B.moe_layer_workspace_bytes(cfg, 1)
         B.moe_set_kernel_path(2)
