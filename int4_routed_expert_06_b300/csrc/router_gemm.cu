@@ -105,16 +105,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool ok = __all_sync(0xFFFFFFFFu, bar_wait(&done, 0) && !s_fail); // tcgen05.ld is warp-collective
     tc_fence_after();
     const int m = m0 + warp * 32 + lane;
+    const bool vec = (E & 3) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0; // rows 16-byte aligned
     if (ok) {
         for (int c0 = 0; c0 < TBN; c0 += 16) {
             uint32_t v[16];
             tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
             if (m < T) {
+                const int nb = n0 + c0;
+                float *row = logits + (size_t)m * E;
+                if (vec && nb + 16 <= E) { // four 16-byte stores
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int n = n0 + c0 + j;
-                    if (n < E)
-                        logits[(size_t)m * E + n] = __uint_as_float(v[j]) + (bias ? bias[n] : 0.f);
+                    for (int j = 0; j < 16; j += 4) {
+                        float4 o;
+                        o.x = __uint_as_float(v[j]) + (bias ? bias[nb + j] : 0.f);
+                        o.y = __uint_as_float(v[j + 1]) + (bias ? bias[nb + j + 1] : 0.f);
+                        o.z = __uint_as_float(v[j + 2]) + (bias ? bias[nb + j + 2] : 0.f);
+                        o.w = __uint_as_float(v[j + 3]) + (bias ? bias[nb + j + 3] : 0.f);
+                        *reinterpret_cast<float4 *>(row + nb + j) = o;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (nb + j < E)
+                            row[nb + j] = __uint_as_float(v[j]) + (bias ? bias[nb + j] : 0.f);
                 }
             }
         }
