@@ -408,7 +408,6 @@ struct GemmArgs {
     int mode;            // 0 gate/up, 1 down
     int H, I, Is, G, T, k;
     int act_ld;          // row length of the activation buffer (max(I, Is))
-    const float *wpair;  // weight of each sorted row (applied by the combine)
     __nv_bfloat16 *act;  // gate/up output [T*k + T, act_ld]
     float *pout;         // down output [T*k + T, H], unweighted
 };
@@ -1062,7 +1061,6 @@ cudaError_t experts_forward(const Shape &s, const ExpertSrc &src, const void *x,
     g.T = T;
     g.k = s.k;
     g.act_ld = imax;
-    g.wpair = wpair;
     g.act = act;
     g.pout = pout;
     g.units = u_gu;
