@@ -134,12 +134,14 @@ def test_layer_decode_parity(name, path, kernel_path):
     assert ties <= 2, f"{ties} near-tie steps of {len(steps)}"
 
 
-@pytest.mark.parametrize("name,T", [("tiny", 4), ("35b-dec", 5), ("80b-dec", 3)])
+@pytest.mark.parametrize("name,T", [("tiny", 4), ("35b-dec", 5), ("80b-dec", 3), ("80b-dec", 12), ("80b-dec", 13)])
 def test_layer_batched_tokens(name, T):
-    """Several tokens in one call (ragged, not a multiple of any tile)."""
+    """Several tokens in one call (ragged, not a multiple of any tile); on the
+    80B layer T = 3 and 12 run the single-token kernels once a token, T = 13
+    the generic kernels."""
     shape, w, L = layer_of(name)
     dl = device_layer(name)
-    x = _xs(name, 8)[:T]
+    x = _xs(name, max(T, 8))[:T]
     y, y32, idx, tw = layer_forward(dl, x)
     ref = L.forward(x)
     ok = ~near_tie_tokens(ref["logits"], shape.top_k)
