@@ -100,14 +100,29 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# the sources of the kernels one prefill layer call launches (router GEMM and
+# shared-gate GEMV, top-k, bucketing, the grouped-GEMM path)
+PREFILL_SOURCES = ("router_gemm.cu", "kernels_decode.cu", "bucket.cu", "prefill.cu")
+
+
+def sources_digest(names) -> str:
+    """sha256 over the named kernel sources, concatenated in the given order."""
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "int4_routed_expert_06_b300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def recorded_traffic(workload: str):
     """DRAM bytes per layer call from the committed ncu capture, or None when
-    the single-token kernel source has changed since the counters were taken."""
-    src = os.path.join(ROOT, "int4_routed_expert_06_b300", "csrc", "kernels_token.cu")
-    rec = os.path.join(ROOT, "profiles", "decode_layer_traffic.txt")
+    the kernel sources have changed since the counters were taken."""
+    if workload == "80b-prefill":
+        srcs, rec = PREFILL_SOURCES, os.path.join(ROOT, "profiles", "prefill_layer_traffic.txt")
+    else:
+        srcs, rec = ("kernels_token.cu",), os.path.join(ROOT, "profiles", "decode_layer_traffic.txt")
     try:
-        with open(src, "rb") as f:
-            digest = hashlib.sha256(f.read()).hexdigest()
+        digest = sources_digest(srcs)
         with open(rec) as f:
             for line in f:
                 parts = line.split()
@@ -368,7 +383,9 @@ def run_prefill(args, shape):
         "roofline": {"kernel": "prefill layer call (router, top-k, bucketing, gather, tcgen05 grouped GEMMs "
                                "gate/up and down, combine), timed as one unit",
                      "bound": "tensor", "achieved": tf, "peak": pk[0], "peak_kind": pk[1], "unit": "TFLOP/s",
-                     "frac": tf / pk[0], "traffic": None, "algorithmic_flops_per_launch": flops},
+                     "frac": tf / pk[0], "traffic": recorded_traffic("80b-prefill"),
+                     "traffic_note": "DRAM bytes of all kernels of one call (ncu, committed record)",
+                     "algorithmic_flops_per_launch": flops},
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": xh.numel() * 2,
                 "d2h_bytes_per_step": yh.numel() * 2},
         "cpu_baseline": cpu,

@@ -2,6 +2,8 @@
 import hashlib
 import os
 
+import pytest
+
 import torch
 
 import bench
@@ -42,13 +44,24 @@ def test_recorded_traffic_needs_the_same_kernel_source(tmp_path, monkeypatch):
     assert bench.recorded_traffic("80b-dec") is None        # source changed since the capture
 
 
-def test_committed_traffic_record_is_well_formed():
-    p = os.path.join(bench.ROOT, "profiles", "decode_layer_traffic.txt")
+@pytest.mark.parametrize("record,workload", [("decode_layer_traffic.txt", "80b-dec"),
+                                             ("prefill_layer_traffic.txt", "80b-prefill")])
+def test_committed_traffic_record_is_well_formed(record, workload):
+    p = os.path.join(bench.ROOT, "profiles", record)
     rows = [l.split() for l in open(p) if l.strip() and not l.startswith("#")]
     assert rows and all(len(r) >= 5 for r in rows)
+    assert any(r[0] == workload for r in rows)
     for r in rows:                      # workload, digest, per-kernel bytes ..., total
         digest, parts, total = r[1], [int(v) for v in r[2:-1]], int(r[-1])
         assert len(digest) == 64 and sum(parts) == total
+
+
+def test_traffic_is_null_once_the_sources_change(monkeypatch):
+    """The record names the kernel sources' digest: a different digest (a
+    changed source) makes the bench report traffic as null."""
+    monkeypatch.setattr(bench, "sources_digest", lambda names: "0" * 64)
+    assert bench.recorded_traffic("80b-dec") is None
+    assert bench.recorded_traffic("80b-prefill") is None
 
 
 def test_stack_layer_input_is_unit_rms_and_scale_free():
