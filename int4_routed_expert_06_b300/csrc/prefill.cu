@@ -2,22 +2,23 @@
 // as grouped GEMMs on the 5th-generation tensor cores (tcgen05, TMEM
 // accumulators, TMA-fed operands).
 //
-//   route      router logits and top-k per token (the generic router kernels)
+//   route      router logits (tcgen05 router GEMM) and top-k per token
 //   bucket     stable counting sort of the T*k (token, rank) pairs by expert
 //   gather     X_sorted[p] = x[token of pair p]           (bf16 rows)
 //   pairs      per sorted row: its routing weight, and the inverse permutation
 //   plan       work units (expert, feature tile, token chunk), largest first
 //   gemm gu    act[p, f] = silu(W_g x_p)_f * (W_u x_p)_f   (bf16)
-//   gemm down  P[p, h]   = w_p * (W_d act_p)_h             (fp32)
-//   combine    y[t] = sum_r P[pair(t, r)] + P[shared row t], fixed order
+//   gemm down  P[p, h]   = (W_d act_p)_h                   (fp32)
+//   combine    y[t] = sum_r w_p P[p] over p = pair(t, r), + g_t P[shared row t],
+//              each product rounded to fp32, summed in that fixed order
 //
 // The GEMMs run "swap-AB": the M = 128 side of each MMA is a tile of weight
-// rows, dequantised from int4 by four warps straight into the 128-byte
-// swizzled K-major shared-memory layout the MMA reads; the N side is the
-// expert's tokens (rounded up to 16, at most 192 per unit), brought in by TMA
-// with the matching swizzle.  Skewed routing then costs at most 15 padded
-// token columns per unit instead of a 128-row tile.  The shared expert is one
-// more group, over all T tokens.
+// rows, dequantised from int4 by 16 warps straight into TMEM (tcgen05.st), the
+// A operand of the MMA; the N side is the expert's tokens (rounded up to 16,
+// at most 192 per unit), brought into shared memory by TMA with a 128-byte
+// swizzle.  Skewed routing then costs at most 15 padded token columns per unit
+// instead of a 128-row tile.  The shared expert is one more group, over all T
+// tokens.
 #include <cuda.h>
 #include <mutex>
 
