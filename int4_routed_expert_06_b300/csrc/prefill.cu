@@ -157,12 +157,6 @@ __host__ __device__ __forceinline__ uint32_t idesc_bf16(int M, int N)
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_commit(uint64_t *bar)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
-}
-
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
 {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -185,20 +179,10 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // D (TMEM) += A (TMEM: 128 lanes = rows, two bf16 of K a column) . B (shared
-// memory descriptor).
-__device__ __forceinline__ void mma_bf16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
-                                            uint32_t accumulate)
-{
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
-                 "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
-                 : "memory");
-}
-
-// The same MMA (and below, the same commit) issued by one lane of a
-// converged warp: elect.sync picks the lowest active lane, so a warp that
-// runs with all lanes always issues from lane 0, and a commit tracks the
-// MMAs that lane issued.
+// memory descriptor), issued by one lane of a converged warp (and below, the
+// commit of the MMAs issued so far): elect.sync picks the lowest active lane,
+// so a warp that runs with all lanes always issues from lane 0, and a commit
+// tracks the MMAs that lane issued.
 __device__ __forceinline__ void mma_bf16_ta_elect(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
                                                   uint32_t accumulate)
 {
